@@ -1,0 +1,42 @@
+"""MLA decode attention in absorbed form, float64.
+
+QuantMLA (Abstract; Figure 8 caption): one query attends to every cached
+token of its sequence; the cached key is the content latent (512) followed by
+the decoupled RoPE key (64); the reconstructed content latent serves both the
+matching (QK) and the latent aggregation (PV) -- the value is the key's first
+512 channels -- and every valid token shares one softmax normalisation.
+
+Adopted readings: the query is already absorbed (``q_nope @ W_UK`` next to the
+rotated ``q_pe``), so the output stays in latent space ``[H][512]`` with no
+up-projection; the softmax scale is given by the caller (1/sqrt(192) in the
+workloads).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .quant import bf16_bits_to_f64
+
+
+def mla_decode_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float):
+    """Softmax attention of ``H`` heads over ``L`` keys.
+
+    ``q_bits``: bf16 bits ``[H][576]``; ``keys``: float64 ``[L][576]``.
+    Returns ``(out [H][512] float64, lse [H] float64)`` where ``lse`` is the
+    natural-log sum of ``exp(logit)``.  With ``L == 0`` the output is zero and
+    ``lse`` is ``-inf``.
+    """
+    q = bf16_bits_to_f64(q_bits)
+    keys = np.asarray(keys, dtype=np.float64)
+    H = q.shape[0]
+    L = keys.shape[0]
+    if L == 0:
+        return np.zeros((H, 512)), np.full(H, -np.inf)
+    z = float(softmax_scale) * (q @ keys.T)          # [H][L]
+    zmax = z.max(axis=1, keepdims=True)
+    e = np.exp(z - zmax)
+    denom = e.sum(axis=1)
+    out = (e @ keys[:, :512]) / denom[:, None]
+    lse = zmax[:, 0] + np.log(denom)
+    return out, lse
