@@ -1,0 +1,418 @@
+"""Benchmark: low-bit MLA decode step on one GB300 (or N replicas under torchrun).
+
+One step = the fused cache writer appending one token per sequence, then the
+split-KV decode (+ log-sum-exp combine) over the whole cache, on the
+DeepSeek-V2-Lite-shaped C4R4 workload (8 sequences x 32768 tokens, 16 heads,
+latent 512 + rope 64, 64-token pages in random physical order) unless
+``--workload`` names another.  Inputs are synthetic and seeded (workloads/).
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
+reference arm; bounded sample of the same workload).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import synthetic as syn  # noqa: E402
+
+METRIC = "C4R4 MLA decode: tokens/s and packed-cache HBM GB/s (% of peak) at 1 GPU"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w: syn.Workload, lens) -> dict:
+    """Bytes the decode must move per step, from the closed form: packed bytes of
+    the packed-served tokens, bf16 bytes of the protected tokens, queries,
+    outputs and block-table entries (split partials are implementation overhead
+    and not counted)."""
+    bpt = {4: 324, 2: 196, 16: 1152}[w.content_bits]
+    packed = w.content_bits != 16
+    tot = 0
+    for L in lens:
+        L = int(L)
+        prot = min(L, 132) if packed else 0
+        tot += (L - prot) * bpt + prot * 1152 + math.ceil(L / 64) * 4
+    tot += w.batch * w.heads * 576 * 2 + w.batch * w.heads * 512 * 4
+    writer = w.batch * (576 * 2 + bpt + (1152 if packed else 0)) if w.writer_in_step else 0
+    return {"decode": tot, "writer": writer}
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock and throttle reasons)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the kernel
+    sources still hash to the value recorded with it."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(os.path.join(ROOT, "bit_mla_kv_lowbit_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "bit_mla_kv_lowbit_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if rec.get("csrc_sha256") != h.hexdigest():
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+class Setup:
+    def __init__(self, w: syn.Workload, dev: str):
+        import torch
+        import bit_mla_kv_lowbit_gb300 as pkg
+        self.torch = torch
+        self.w = w
+        self.dev = dev
+        self.lens = syn.sequence_lengths(w).astype(np.int32)
+        self.table, self.npages = syn.make_paging(w)
+        self.cache = pkg.PagedCache(w.content_bits, w.rope_bits, self.table, self.npages, dev)
+        scales = syn.channel_scales(w)
+        B = w.batch
+        new_ckv = np.empty((B, 512), np.uint16)
+        new_kr = np.empty((B, 64), np.uint16)
+        lens_prev = (self.lens - 1).astype(np.int32)
+        lens_prev_d = torch.from_numpy(lens_prev).to(dev)
+        for b in range(B):
+            ckv, kr = syn.sequence_tokens(w, b, scales=scales)
+            n = int(self.lens[b]) - 1
+            new_ckv[b], new_kr[b] = ckv[n], kr[n]
+            if n > 0:
+                self.cache.write(torch.from_numpy(ckv[:n]).to(dev).view(torch.bfloat16),
+                                 torch.from_numpy(kr[:n]).to(dev).view(torch.bfloat16),
+                                 torch.arange(n, dtype=torch.int32, device=dev),
+                                 seq_idx=torch.full((n,), b, dtype=torch.int32, device=dev),
+                                 seq_lens_after=lens_prev_d)
+            del ckv, kr
+        q = np.stack([syn.queries(w, b)[0] for b in range(B)])
+        self.h_q = torch.from_numpy(q).view(torch.bfloat16).pin_memory()
+        self.h_ckv = torch.from_numpy(new_ckv).view(torch.bfloat16).pin_memory()
+        self.h_kr = torch.from_numpy(new_kr).view(torch.bfloat16).pin_memory()
+        self.q = self.h_q.to(dev)
+        self.ckv = self.h_ckv.to(dev)
+        self.kr = self.h_kr.to(dev)
+        self.pos = torch.from_numpy(self.lens - 1).to(dev)
+        self.lens_d = torch.from_numpy(self.lens).to(dev)
+        self.lens_h = [int(x) for x in self.lens]
+        self.out = torch.empty(B, w.heads, 512, dtype=torch.float32, device=dev)
+        self.h_out = torch.empty(B, w.heads, 512, dtype=torch.float32).pin_memory()
+        self.ws = self.cache.workspace(w.heads, self.lens_h)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        assert self.cache.error() == 0, "device error during prefill"
+
+    def write(self):
+        if self.w.writer_in_step:
+            self.cache.write(self.ckv, self.kr, self.pos, seq_lens_after=self.lens_d)
+
+    def decode(self):
+        self.cache.decode(self.q, self.lens_d, self.lens_h, self.w.softmax_scale, out=self.out,
+                          workspace=self.ws)
+
+    def step(self):
+        self.write()
+        self.decode()
+
+    def step_e2e(self):
+        """Same step through the public API from pinned host buffers."""
+        self.q.copy_(self.h_q, non_blocking=True)
+        if self.w.writer_in_step:
+            self.ckv.copy_(self.h_ckv, non_blocking=True)
+            self.kr.copy_(self.h_kr, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def run_gpu(args, w):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    s = Setup(w, dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        s.step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region: K steps, L2 flushed between them
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            s.flush.zero_()
+            ev[i][0].record(stream)
+            s.write()
+            ev[i][1].record(stream)
+            s.decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+
+    # ---- end to end through the public API with host buffers
+    for _ in range(2):
+        s.step_e2e()
+    torch.cuda.synchronize()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        s.flush.zero_()
+        ev2[i][0].record(stream)
+        s.step_e2e()
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = [a.elapsed_time(b) for a, b in ev2]
+    assert s.cache.error() == 0, f"device error word {s.cache.error()}"
+
+    t_step = sum(step_ms) / len(step_ms)
+    t_dec = sum(dec_ms) / len(dec_ms)
+    t_e2e = sum(e2e_ms) / len(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([t_step, t_dec, t_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_dec, t_e2e = t.tolist()
+    B = w.batch
+    tokens_per_s = world * B / (t_step * 1e-3)
+    e2e_tokens_per_s = world * B / (t_e2e * 1e-3)
+    by = algorithmic_bytes(w, s.lens)
+    peak, peak_kind = peaks()
+    dec_gbs = by["decode"] / (t_dec * 1e-3) / 1e9
+    trec = traffic_record(f"decode_{w.name}")
+    n_launch_step = (1 if w.writer_in_step else 0) + 2
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(tokens_per_s, 1),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(t_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16-mma/f32 (int codes exact)",
+            "data": "synthetic (seeded; workloads/synthetic.py)",
+            "config": {"workload": w.name, "batch_per_gpu": B, "heads": w.heads,
+                       "context": [int(x) for x in s.lens][:8],
+                       "layout": f"C{w.content_bits}R{w.rope_bits}" if w.content_bits != 16
+                       else "bf16", "page_tokens": 64, "writer_in_step": w.writer_in_step,
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "packed_cache_gbs": round(dec_gbs, 1),
+            "hbm_frac": round(dec_gbs / peak, 4),
+            "decode_us": round(t_dec * 1e3, 2),
+            "kv_tokens_per_s": round(world * float(np.sum(s.lens)) / (t_step * 1e-3), 1),
+            "roofline": {"bound": "hbm" if w.heads <= 32 or w.content_bits == 16 else "tensor",
+                         "kernel": "decode (split + combine)",
+                         "achieved": round(dec_gbs, 1), "peak": peak,
+                         "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                         "frac": round(dec_gbs / peak, 4),
+                         "algorithmic_bytes": by["decode"],
+                         "traffic": (trec or {}).get("dram_bytes_per_launch")},
+            "e2e": {"value": round(e2e_tokens_per_s, 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(s.h_q.numel() * 2 + (
+                        (s.h_ckv.numel() + s.h_kr.numel()) * 2 if w.writer_in_step else 0)),
+                    "d2h_bytes_per_step": int(s.h_out.numel() * 4)},
+            "gpu_launches": n_launch_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- the oracle arm
+
+def _oracle_sample(w: syn.Workload):
+    """Oracle state for sequence 0 of the workload (prefilled, not timed)."""
+    import oracle
+    lens = syn.sequence_lengths(w)
+    table, npages = syn.make_paging(w)
+    b = 0
+    L = int(lens[b])
+    ckv, kr = syn.sequence_tokens(w, b)
+    lay = oracle.Layout(w.content_bits, w.rope_bits)
+    model = oracle.PagedCacheModel(lay, npages, table)
+    lens_after = np.zeros(w.batch, np.int64)
+    lens_after[b] = L - 1
+    model.write(np.full(L - 1, b), np.arange(L - 1), ckv[:L - 1], kr[:L - 1], lens_after)
+    q = syn.queries(w, b)[0]
+    return model, b, L, ckv[L - 1:L], kr[L - 1:L], q
+
+
+def _oracle_step(w, model, b, L, ckv1, kr1, q):
+    import oracle
+    lens_after = np.zeros(w.batch, np.int64)
+    lens_after[b] = L
+    if w.writer_in_step:
+        model.write([b], [L - 1], ckv1, kr1, lens_after)
+    return oracle.mla_decode_fp64(q, model.effective_keys(b, L), w.softmax_scale)
+
+
+def cpu_baseline(w: syn.Workload, budget_s: float):
+    """The oracle as it stands, timed on this host for one sequence per step,
+    repeated until ``budget_s`` seconds; tokens/s = output tokens / time."""
+    model, b, L, ckv1, kr1, q = _oracle_sample(w)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(w, model, b, L, ckv1, kr1, q)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(n / el, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} decode steps of sequence 0 (L={L}, {w.heads} heads"
+                      f"{', writer + ' if w.writer_in_step else ', '}fp64 attention) of "
+                      f"{w.name}, {el:.1f} s"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    model, b, L, ckv1, kr1, q = _oracle_sample(w)
+    for _ in range(max(args.warmup, 0)):
+        _oracle_step(w, model, b, L, ckv1, kr1, q)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, model, b, L, ckv1, kr1, q)
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; workloads/synthetic.py)",
+        "config": {"workload": w.name, "batch_per_gpu": w.batch, "heads": w.heads,
+                   "sample": "sequence 0 per step (CPU oracle)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} decode steps of sequence 0 (L={L})"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = syn.get(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

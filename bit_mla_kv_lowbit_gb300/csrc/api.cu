@@ -1,0 +1,200 @@
+// Host side of the C ABI declared in include/mla_lowbit.h: argument checks,
+// split planning and kernel launches.  No device memory is allocated here.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace mlalb {
+
+namespace {
+
+constexpr int kMaxHeads = 128;
+constexpr int kCtasPerSm = 2;
+
+int check_layout(const mla_lowbit_layout* l) {
+  if (!l) return MLA_LOWBIT_ENULL;
+  const bool ok_bits = (l->content_bits == 4 && l->rope_bits == 4) ||
+                       (l->content_bits == 2 && l->rope_bits == 4) ||
+                       (l->content_bits == 16 && l->rope_bits == 16);
+  if (!ok_bits || l->group != kGroup || l->sink != kSink || l->local != kLocal ||
+      l->page_tokens != kPageTokens || l->latent != kLatent || l->rope != kRope)
+    return MLA_LOWBIT_EINVAL;
+  return MLA_LOWBIT_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+}  // namespace mlalb
+
+using namespace mlalb;
+
+extern "C" {
+
+size_t mla_lowbit_page_bytes(const mla_lowbit_layout* layout) {
+  if (check_layout(layout) != MLA_LOWBIT_OK) return 0;
+  return static_cast<size_t>(page_geom(layout->content_bits).page_bytes);
+}
+
+size_t mla_lowbit_bytes_per_token(const mla_lowbit_layout* layout) {
+  if (check_layout(layout) != MLA_LOWBIT_OK) return 0;
+  return mla_lowbit_page_bytes(layout) / kPageTokens;
+}
+
+int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* ckv,
+                     const void* krope, const int32_t* seq_idx, const int32_t* pos,
+                     const int32_t* seq_lens_after, int num_seqs, const int32_t* block_table,
+                     int max_pages, void* page_pool, int64_t num_pages, void* sink_buf,
+                     void* recent_buf, int32_t* err_word, void* stream) {
+  int st = check_layout(layout);
+  if (st != MLA_LOWBIT_OK) return st;
+  if (n_tokens < 0 || num_seqs < 0 || max_pages < 0 || num_pages < 0) return MLA_LOWBIT_ESIZE;
+  if (n_tokens == 0) return MLA_LOWBIT_OK;
+  if (num_seqs == 0 || max_pages == 0 || num_pages == 0) return MLA_LOWBIT_ESIZE;
+  if ((long long)max_pages * kPageTokens > INT32_MAX) return MLA_LOWBIT_ESIZE;
+  const bool packed = layout->content_bits != 16;
+  if (!ckv || !krope || !pos || !block_table || !page_pool || !err_word) return MLA_LOWBIT_ENULL;
+  if (!seq_idx && n_tokens > num_seqs) return MLA_LOWBIT_EINVAL;
+  if (packed && (!sink_buf || !recent_buf)) return MLA_LOWBIT_ENULL;
+  if (!aligned16(ckv) || !aligned16(krope) || !aligned16(page_pool) ||
+      (packed && (!aligned16(sink_buf) || !aligned16(recent_buf))))
+    return MLA_LOWBIT_EALIGN;
+  WriterArgs a;
+  a.ckv = static_cast<const uint32_t*>(ckv);
+  a.krope = static_cast<const uint32_t*>(krope);
+  a.seq_idx = seq_idx;
+  a.pos = pos;
+  a.lens_after = seq_lens_after;
+  a.block_table = block_table;
+  a.pool = static_cast<uint8_t*>(page_pool);
+  a.sink = static_cast<uint32_t*>(sink_buf);
+  a.recent = static_cast<uint32_t*>(recent_buf);
+  a.err = err_word;
+  a.num_pages = num_pages;
+  a.n_tokens = n_tokens;
+  a.num_seqs = num_seqs;
+  a.max_pages = max_pages;
+  cudaError_t e = launch_writer(layout->content_bits, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_LOWBIT_OK : MLA_LOWBIT_ECUDA;
+}
+
+int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                           const int32_t* seq_lens_host, int num_sms, int* total_splits,
+                           int* chunk_pages, size_t* workspace_bytes) {
+  int st = check_layout(layout);
+  if (st != MLA_LOWBIT_OK) return st;
+  if (num_seqs <= 0 || heads <= 0 || heads % 16 != 0 || heads > kMaxHeads) return MLA_LOWBIT_ESIZE;
+  if (!seq_lens_host || !total_splits || !chunk_pages || !workspace_bytes) return MLA_LOWBIT_ENULL;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return MLA_LOWBIT_ECUDA;
+  const bool packed = layout->content_bits != 16;
+  long long work = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    if (seq_lens_host[b] < 0) return MLA_LOWBIT_EINVAL;
+    work += packed_pages_of(seq_lens_host[b], packed);
+  }
+  const long long head_chunks = heads / 16;
+  const long long slots = (long long)num_sms * kCtasPerSm;
+  long long chunk = (work * head_chunks + slots - 1) / slots;
+  if (chunk < 1) chunk = 1;
+  if (chunk > (1 << 20)) chunk = 1 << 20;
+  long long total = 0;
+  for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
+  if (total > INT32_MAX / 2) return MLA_LOWBIT_ESIZE;
+  *total_splits = (int)total;
+  *chunk_pages = (int)chunk;
+  const size_t part = (size_t)total * heads * (kLatent + 2) * sizeof(float);
+  *workspace_bytes = part + (size_t)num_seqs * 2 * sizeof(int32_t);
+  return MLA_LOWBIT_OK;
+}
+
+int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                      float softmax_scale, const void* q, const void* page_pool,
+                      int64_t num_pages, const int32_t* block_table, int max_pages,
+                      const int32_t* seq_lens, const int32_t* seq_lens_host,
+                      const void* sink_buf, const void* recent_buf, float* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int32_t* err_word,
+                      void* stream) {
+  int st = check_layout(layout);
+  if (st != MLA_LOWBIT_OK) return st;
+  if (num_seqs <= 0 || heads <= 0 || heads % 16 != 0 || heads > kMaxHeads || max_pages <= 0 ||
+      num_pages <= 0)
+    return MLA_LOWBIT_ESIZE;
+  if ((long long)max_pages * kPageTokens > INT32_MAX) return MLA_LOWBIT_ESIZE;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MLA_LOWBIT_EINVAL;
+  const bool packed = layout->content_bits != 16;
+  if (!q || !page_pool || !block_table || !seq_lens || !seq_lens_host || !out || !workspace ||
+      !err_word)
+    return MLA_LOWBIT_ENULL;
+  if (packed && (!sink_buf || !recent_buf)) return MLA_LOWBIT_ENULL;
+  if (!aligned16(q) || !aligned16(page_pool) || !aligned16(out) || !aligned16(workspace) ||
+      (packed && (!aligned16(sink_buf) || !aligned16(recent_buf))))
+    return MLA_LOWBIT_EALIGN;
+  for (int b = 0; b < num_seqs; ++b)
+    if (seq_lens_host[b] < 0 || (long long)seq_lens_host[b] > (long long)max_pages * kPageTokens)
+      return MLA_LOWBIT_EINVAL;
+  int total = 0, chunk = 0;
+  size_t need = 0;
+  st = mla_lowbit_decode_plan(layout, num_seqs, heads, seq_lens_host, 0, &total, &chunk, &need);
+  if (st != MLA_LOWBIT_OK) return st;
+  if (workspace_bytes < need) return MLA_LOWBIT_EWORKSPACE;
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.pool = static_cast<const uint8_t*>(page_pool);
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.sink = static_cast<const uint16_t*>(sink_buf);
+  a.recent = static_cast<const uint16_t*>(recent_buf);
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = a.part_o + (size_t)total * heads * kLatent;
+  a.seq_split = reinterpret_cast<int32_t*>(a.part_ml + (size_t)total * heads * 2);
+  a.err = err_word;
+  a.B = num_seqs;
+  a.H = heads;
+  a.max_pages = max_pages;
+  a.chunk_pages = chunk;
+  a.total_splits = total;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e =
+      launch_decode(layout->content_bits, a, out, lse, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_LOWBIT_OK : MLA_LOWBIT_ECUDA;
+}
+
+int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out) {
+  if (!err_word || !code_out) return MLA_LOWBIT_ENULL;
+  return cudaMemcpy(code_out, err_word, sizeof(int32_t), cudaMemcpyDeviceToHost) == cudaSuccess
+             ? MLA_LOWBIT_OK
+             : MLA_LOWBIT_ECUDA;
+}
+
+const char* mla_lowbit_strerror(int status) {
+  switch (status) {
+    case MLA_LOWBIT_OK: return "ok";
+    case MLA_LOWBIT_EINVAL: return "invalid layout or argument value";
+    case MLA_LOWBIT_ENULL: return "required pointer is NULL";
+    case MLA_LOWBIT_EALIGN: return "pointer is not 16-byte aligned";
+    case MLA_LOWBIT_ESIZE: return "size outside the supported range";
+    case MLA_LOWBIT_EWORKSPACE: return "workspace smaller than the decode plan needs";
+    case MLA_LOWBIT_ECUDA: return "CUDA runtime call or kernel launch failed";
+    default: return "unknown status";
+  }
+}
+
+int mla_lowbit_version(void) { return 100; }
+
+}  // extern "C"

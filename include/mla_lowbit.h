@@ -1,0 +1,183 @@
+/*
+ * mla_lowbit.h -- C ABI of the low-bit MLA decode library (one GB300, sm_103a).
+ *
+ * What it computes follows "QuantMLA: Function-Aligned Dual-Path Quantization
+ * for Low-Bit MLA KV Caching":
+ *   - Abstract: the content latent (c_kv, 512 channels) is cached at INT4 or
+ *     INT2 and the decoupled RoPE key (64 channels) at INT4; a native low-bit
+ *     MLA attention kernel unpacks and dequantises inside attention;
+ *   - Figure 3 caption: the backend stores packed cache representations and
+ *     serves protected sink and recent tokens from bf16 buffers;
+ *   - Figure 8 caption: a fused writer packs every incoming token and keeps the
+ *     bf16 values of protected tokens; attention uses the bf16 values for
+ *     protected tokens and dequantised values otherwise; the reconstructed
+ *     content tile serves both matching (QK) and latent aggregation (PV); all
+ *     valid tokens share one softmax normalisation;
+ *   - Figure 5 / Table 9 captions: the protection policy is sink 4 / local 128.
+ * The pages leave the quantiser open; this library fixes it as per-token
+ * asymmetric quantisation over 64-channel groups with an fp16 scale and an fp16
+ * min per group and round-half-to-even codes (details at mla_lowbit_write).
+ *
+ * Conventions for every call:
+ *   - All tensors are device pointers unless marked "host".  The caller owns
+ *     all memory; the library never allocates or frees device memory.
+ *   - Calls are asynchronous on the caller's stream (`stream` is a
+ *     cudaStream_t; NULL means the legacy default stream).
+ *   - Return value: MLA_LOWBIT_OK or a negative MLA_LOWBIT_E* status for errors
+ *     found on the host (bad layout, NULL pointer, misalignment, size, small
+ *     workspace, launch failure).  Nothing is launched when a call fails.
+ *   - Errors that only the device can see (a page id outside the pool, a
+ *     position outside the block table, a sequence length out of range) are
+ *     OR-ed into the int32 `err_word` (device memory, MLA_LOWBIT_DEV_* bits);
+ *     the offending work is skipped, never trapped.  Read it with
+ *     mla_lowbit_read_error.
+ *   - Pointers to the page pool, bf16 buffers, queries, outputs and the
+ *     workspace must be 16-byte aligned.
+ */
+#ifndef MLA_LOWBIT_H
+#define MLA_LOWBIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Cache layout.  Supported (content_bits, rope_bits): (4,4) "C4R4", (2,4)
+ * "C2R4", (16,16) unquantised bf16 pages.  The other fields must hold the
+ * values shown (they are checked, so a caller states its assumptions). */
+typedef struct mla_lowbit_layout {
+  int content_bits; /* 4, 2, or 16 (bf16 pages) */
+  int rope_bits;    /* 4, or 16 with bf16 pages */
+  int group;        /* 64: channels per quantisation group */
+  int sink;         /* 4: leading tokens kept in bf16 */
+  int local;        /* 128: trailing tokens kept in bf16 */
+  int page_tokens;  /* 64: tokens per page */
+  int latent;       /* 512: content latent width (kv_lora_rank) */
+  int rope;         /* 64: RoPE key width (qk_rope_head_dim) */
+} mla_lowbit_layout;
+
+enum {
+  MLA_LOWBIT_OK = 0,
+  MLA_LOWBIT_EINVAL = -1,     /* bad layout or argument value */
+  MLA_LOWBIT_ENULL = -2,      /* required pointer is NULL */
+  MLA_LOWBIT_EALIGN = -3,     /* pointer not 16-byte aligned */
+  MLA_LOWBIT_ESIZE = -4,      /* size outside the supported range */
+  MLA_LOWBIT_EWORKSPACE = -5, /* workspace smaller than the plan needs */
+  MLA_LOWBIT_ECUDA = -6       /* a CUDA runtime call or launch failed */
+};
+
+/* Bits OR-ed into the device error word. */
+enum {
+  MLA_LOWBIT_DEV_BAD_SEQ = 1,   /* writer: sequence index outside [0, num_seqs) */
+  MLA_LOWBIT_DEV_BAD_POS = 2,   /* position < 0 or >= max_pages * 64 */
+  MLA_LOWBIT_DEV_BAD_PAGE = 4,  /* block-table entry outside [0, num_pages) */
+  MLA_LOWBIT_DEV_BAD_LEN = 8,   /* decode: seq_len < 0 or > max_pages * 64 */
+  MLA_LOWBIT_DEV_PLAN = 16      /* decode: device lengths disagree with seq_lens_host */
+};
+
+/* Bytes of one 64-token page: 20736 (C4R4), 12544 (C2R4), 73728 (bf16).
+ * Page layout (every region starts on a 128-byte boundary):
+ *   packed: content codes [64][latent*content_bits/8] u8, then RoPE codes
+ *           [64][rope*rope_bits/8] u8, then metadata [64][9] x {fp16 scale,
+ *           fp16 min} (groups 0..7 content, 8 RoPE);
+ *           INT4: channel 2i -> low nibble of byte i, 2i+1 -> high nibble;
+ *           INT2: channel 4i+j -> bits 2j..2j+1 of byte i;
+ *   bf16:   [64][576] bf16 (content then RoPE), no metadata.
+ * Returns 0 for an unsupported layout. */
+size_t mla_lowbit_page_bytes(const mla_lowbit_layout* layout);
+
+/* Packed bytes per cached token: 324 (C4R4), 196 (C2R4), 1152 (bf16). */
+size_t mla_lowbit_bytes_per_token(const mla_lowbit_layout* layout);
+
+/* Fused cache writer (Figure 8 caption: each arriving token is packed, and the
+ * bf16 values of protected tokens are kept in their own buffers).
+ *
+ * Token i (0 <= i < n_tokens) has content latent ckv[i][512] and RoPE key
+ * krope[i][64] (bf16, already rotated), sequence seq_idx[i] (or i when seq_idx
+ * is NULL) and position pos[i].  It is stored in page block_table[s][pos/64],
+ * row pos%64.  For packed layouts each of its 9 groups of 64 channels is
+ * quantised with bits b (content_bits for groups 0..7, rope_bits for group 8):
+ *   mn, mx = min, max of the group (float32);
+ *   s16 = fp16_rn(min((mx - mn) / (2^b - 1), 65504)), m16 = fp16_rn(mn clamped
+ *   to +-65504), both float32 operations rounded to nearest;
+ *   code = clamp(round_half_even((x - m16) / s16), 0, 2^b - 1) with float32
+ *   subtraction and true division; every code is 0 when s16 == 0.
+ * A packed copy is written for every token, protected or not.  In addition
+ * (packed layouts only) a token with pos < 4 is copied to sink_buf[s][pos] and
+ * a token with pos >= seq_lens_after[s] - 128 to recent_buf[s][pos % 128]
+ * (seq_lens_after == NULL means pos[i] + 1, the one-token decode step).  Within
+ * one call the positions of a sequence must be distinct.
+ *
+ *   ckv            [n_tokens][512] bf16        krope   [n_tokens][64] bf16
+ *   seq_idx        [n_tokens] int32 or NULL    pos     [n_tokens] int32
+ *   seq_lens_after [num_seqs] int32 or NULL
+ *   block_table    [num_seqs][max_pages] int32 (physical page ids)
+ *   page_pool      [num_pages][page_bytes] u8
+ *   sink_buf       [num_seqs][4][576] bf16, recent_buf [num_seqs][128][576]
+ *                  bf16 (may be NULL for bf16 pages)
+ *   err_word       int32 (device), OR-ed MLA_LOWBIT_DEV_* bits
+ */
+int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* ckv,
+                     const void* krope, const int32_t* seq_idx, const int32_t* pos,
+                     const int32_t* seq_lens_after, int num_seqs, const int32_t* block_table,
+                     int max_pages, void* page_pool, int64_t num_pages, void* sink_buf,
+                     void* recent_buf, int32_t* err_word, void* stream);
+
+/* Split-KV plan of one decode call.  Pages of each sequence are cut into
+ * splits of `chunk_pages` pages (chosen from the total work and the SM count);
+ * packed layouts add one split per sequence for its bf16 tokens.  Writes the
+ * number of splits and the workspace bytes the call needs.  num_sms == 0 asks
+ * the current CUDA device. */
+int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                           const int32_t* seq_lens_host, int num_sms, int* total_splits,
+                           int* chunk_pages, size_t* workspace_bytes);
+
+/* Low-bit MLA decode attention in absorbed form (Abstract: unpacking and
+ * dequantisation inside attention; Figure 8 caption: bf16 values for
+ * protected tokens, one global softmax, the content tile used for QK and PV).
+ *
+ * For sequence s with L = seq_lens[s] cached tokens and head h:
+ *   key_t  = bf16 value of token t if t < 4 or t >= L - 128 (sink/recent
+ *            buffers), else s16*code + m16 from its packed page (bf16 pages:
+ *            always the page value);
+ *   z_t    = softmax_scale * dot(q[s][h][0:576], key_t[0:576]);
+ *   out[s][h][c] = sum_t softmax(z)_t * key_t[c],  c < 512 (value = latent);
+ *   lse[s][h]    = log(sum_t exp(z_t)) (natural log; -inf and out = 0 when L = 0).
+ * heads must be a multiple of 16, at most 128.
+ *
+ *   q             [num_seqs][heads][576] bf16
+ *   page_pool     [num_pages][page_bytes] u8 (as written by mla_lowbit_write)
+ *   block_table   [num_seqs][max_pages] int32
+ *   seq_lens      [num_seqs] int32 (device) and seq_lens_host (host, same
+ *                 values; used to plan the split grid)
+ *   sink_buf, recent_buf as for the writer (ignored for bf16 pages)
+ *   out           [num_seqs][heads][512] float32
+ *   lse           [num_seqs][heads] float32, or NULL
+ *   workspace     at least the bytes mla_lowbit_decode_plan reports
+ *   err_word      int32 (device), OR-ed MLA_LOWBIT_DEV_* bits
+ * Launches the split kernel and the log-sum-exp combine kernel on `stream`. */
+int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                      float softmax_scale, const void* q, const void* page_pool,
+                      int64_t num_pages, const int32_t* block_table, int max_pages,
+                      const int32_t* seq_lens, const int32_t* seq_lens_host,
+                      const void* sink_buf, const void* recent_buf, float* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int32_t* err_word,
+                      void* stream);
+
+/* Synchronously copies the device error word to *code_out (a blocking
+ * cudaMemcpy: it waits for prior work on the legacy default stream). */
+int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out);
+
+/* Human-readable text for a status code; never NULL. */
+const char* mla_lowbit_strerror(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int mla_lowbit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_LOWBIT_H */

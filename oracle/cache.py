@@ -12,7 +12,7 @@ Readings adopted where the pages are silent:
 * the window counts the token just written: with ``L`` tokens held, token ``t``
   is protected iff ``t < 4`` or ``t >= L - 128``;
 * for ``L <= 132`` every token is protected (the two rules overlap);
-* sink tokens get packed copies too ("every incoming token");
+* sink tokens get packed copies too (the writer packs all tokens alike);
 * the recent buffer is a ring of 128 rows indexed by ``pos mod 128``; within one
   write call a token reaches the ring only if it is among the last 128 of its
   sequence after the call, so a bulk prefill leaves the same ring as

@@ -6,7 +6,8 @@ every incoming token.  The pages do not fix the quantiser; the adopted
 definition (an RTN-style asymmetric quantiser, named as a baseline in Table 3)
 is, per token and per 64-channel group, in this order:
 
-1. ``mn, mx`` = min and max of the group's bf16 values (exact in float32);
+1. ``mn, mx`` = min and max of the group's bf16 values (exact in float32); a
+   zero minimum is taken as +0, so the stored fp16 min never holds -0;
 2. ``s32 = float32(mx - mn) / float32(2**bits - 1)`` (IEEE float32, nearest);
 3. ``s16 = fp16(s32)``, ``m16 = fp16(mn)``: nearest-even, saturating at +-65504;
 4. ``r = float32(x - float32(m16)) / float32(s16)`` (two float32 operations,
@@ -51,7 +52,7 @@ def quantize_group(x_bits: np.ndarray, bits: int):
     if np.any(~np.isfinite(x)) or np.any(np.abs(x) > F16_MAX):
         raise ValueError("input outside the fp16 metadata range (|x| > 65504)")
     levels = np.float32(2 ** bits - 1)
-    mn = x.min(axis=-1)
+    mn = x.min(axis=-1) + np.float32(0.0)   # -0 + 0 = +0 under round-to-nearest
     mx = x.max(axis=-1)
     s32 = np.subtract(mx, mn, dtype=np.float32) / levels
     s16 = f16_satfinite(s32)

@@ -1,0 +1,145 @@
+"""Host-side checks of the C ABI that need no GPU: symbols, sizes, argument
+validation and split planning."""
+
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bit_mla_kv_lowbit_gb300 as pkg
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_lowbit.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_lowbit_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pkg.load()
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in mla_lowbit.h but not exported"
+    assert set(names) == set(pkg.EXPORTS)
+
+
+def test_sizes_agree_with_oracle_closed_form():
+    for cb, rb in ((4, 4), (2, 4), (16, 16)):
+        lay = pkg.layout(cb, rb)
+        olay = oracle.Layout(cb, rb)
+        assert pkg.page_bytes(lay) == oracle.page_geometry(olay)["page_bytes"]
+        assert pkg.bytes_per_token(lay) == oracle.bytes_per_token(olay)
+
+
+@pytest.mark.parametrize("fields", [
+    dict(content_bits=3), dict(rope_bits=2), dict(group=32), dict(sink=0), dict(local=64),
+    dict(page_tokens=128), dict(latent=256), dict(rope=32),
+])
+def test_invalid_layouts_rejected(fields):
+    lay = pkg.layout(4, 4)
+    for k, v in fields.items():
+        setattr(lay, k, v)
+    assert pkg.page_bytes(lay) == 0
+    with pytest.raises(pkg.LibraryError):
+        pkg.decode_plan(lay, 16, [100], num_sms=152)
+
+
+def test_strerror_and_version():
+    assert pkg.strerror(0) == "ok"
+    for st in range(-6, 0):
+        assert pkg.strerror(st) != "unknown status"
+    assert pkg.strerror(-99) == "unknown status"
+    assert pkg.version() >= 100
+
+
+def _call_write(lay, **over):
+    lib = pkg.load()
+    args = dict(n=4, ckv=0x1000, krope=0x2000, seq_idx=None, pos=0x3000, lens=None, num_seqs=4,
+                table=0x4000, max_pages=8, pool=0x5000, num_pages=16, sink=0x6000,
+                recent=0x7000, err=0x8000, stream=None)
+    args.update(over)
+    return lib.mla_lowbit_write(ctypes.byref(lay), args["n"], args["ckv"], args["krope"],
+                                args["seq_idx"], args["pos"], args["lens"], args["num_seqs"],
+                                args["table"], args["max_pages"], args["pool"], args["num_pages"],
+                                args["sink"], args["recent"], args["err"], args["stream"])
+
+
+def test_write_host_validation_without_launch():
+    lay = pkg.layout(4, 4)
+    assert _call_write(lay, n=0) == 0                 # nothing to do
+    assert _call_write(lay, ckv=None) == -2
+    assert _call_write(lay, err=None) == -2
+    assert _call_write(lay, sink=None) == -2
+    assert _call_write(lay, pool=0x5004) == -3        # misaligned
+    assert _call_write(lay, n=-1) == -4
+    assert _call_write(lay, n=5, num_seqs=4) == -1    # identity seq_idx needs n <= num_seqs
+    assert _call_write(pkg.layout(16, 16), sink=None, recent=None, ckv=None) == -2
+    bad = pkg.layout(4, 4)
+    bad.content_bits = 8
+    assert _call_write(bad) == -1
+
+
+def _call_decode(lay, **over):
+    lib = pkg.load()
+    lens = np.array([100, 200], np.int32)
+    args = dict(B=2, H=16, scale=0.07, q=0x1000, pool=0x2000, num_pages=8, table=0x3000,
+                max_pages=4, lens=0x4000, lens_host=lens.ctypes.data, sink=0x5000, recent=0x6000,
+                out=0x7000, lse=None, ws=0x8000, ws_bytes=1 << 30, err=0x9000, stream=None)
+    args.update(over)
+    return lib.mla_lowbit_decode(ctypes.byref(lay), args["B"], args["H"],
+                                 ctypes.c_float(args["scale"]), args["q"], args["pool"],
+                                 args["num_pages"], args["table"], args["max_pages"], args["lens"],
+                                 args["lens_host"], args["sink"], args["recent"], args["out"],
+                                 args["lse"], args["ws"], args["ws_bytes"], args["err"],
+                                 args["stream"])
+
+
+def test_decode_host_validation_without_launch():
+    lay = pkg.layout(4, 4)
+    assert _call_decode(lay, H=24) == -4
+    assert _call_decode(lay, H=144) == -4
+    assert _call_decode(lay, B=0) == -4
+    assert _call_decode(lay, q=None) == -2
+    assert _call_decode(lay, lens_host=None) == -2
+    assert _call_decode(lay, out=0x7008) == -3
+    assert _call_decode(lay, scale=0.0) == -1
+    assert _call_decode(lay, scale=float("nan")) == -1
+    too_long = np.array([100, 4 * 64 + 1], np.int32)
+    assert _call_decode(lay, lens_host=too_long.ctypes.data) == -1
+
+
+def _expected_splits(L, packed, chunk):
+    # Packed layouts: pages that hold at least one token served from packed codes
+    # (positions 4 .. L-129), cut into chunks, plus one split for the bf16 tokens.
+    if packed:
+        served = [t for t in range(4, max(4, L - 128))]
+        pages = len({t // 64 for t in served})
+        return math.ceil(pages / chunk) + 1
+    pages = math.ceil(L / 64)
+    return max(1, math.ceil(pages / chunk))
+
+
+@pytest.mark.parametrize("cb", [4, 2, 16])
+def test_plan_matches_definition(cb):
+    lay = pkg.layout(cb, 4 if cb != 16 else 16)
+    rng = np.random.default_rng(0)
+    lens = [0, 1, 4, 5, 131, 132, 133, 192, 193, 196, 197, 260, 1000, 4099]
+    lens += rng.integers(0, 20000, 10).tolist()
+    for heads in (16, 64, 128):
+        total, chunk, ws = pkg.decode_plan(lay, heads, lens, num_sms=152)
+        assert chunk >= 1
+        assert total == sum(_expected_splits(L, cb != 16, chunk) for L in lens)
+        assert ws == total * heads * (512 + 2) * 4 + len(lens) * 8
+
+
+def test_plan_fills_one_wave_on_uniform_lengths():
+    total, chunk, _ = pkg.decode_plan(pkg.layout(4, 4), 16, [32768] * 8, num_sms=152)
+    assert total <= 2 * 152 and total >= 2 * 152 - 8

@@ -147,6 +147,14 @@ def test_code_range_and_error_bound(bits):
     assert np.all(np.abs(xh - xf).max(1) <= bound)
 
 
+def test_zero_minimum_is_stored_as_plus_zero():
+    x = np.zeros(64, np.float32)
+    x[3] = -0.0
+    x[7] = 2.0
+    codes, s16, m16 = oracle.quantize_group(bf16(x), 4)
+    assert m16.view(np.uint16) == 0 and float(s16) == np.float16(2.0 / 15)
+
+
 def test_out_of_contract_inputs_raise():
     x = np.zeros(64, np.float32)
     x[5] = 65536.0   # bf16-representable, beyond fp16
