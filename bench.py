@@ -63,58 +63,62 @@ def algorithmic_bytes(w: syn.Workload, lens) -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region (SM clock and throttle reasons)."""
+    """Polls nvidia-smi (SM clock, max clock, throttle reasons) in a thread.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Started before the warm-up; ``mark()`` brackets the timed region and the
+    summary uses the samples taken inside it (or the nearest ones when the
+    region is shorter than one poll)."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
-        self.proc = None
-        self.lines = []
+        self.samples = []  # (t, sm, max, reasons)
+        self.stop = threading.Event()
+        self.window = [None, None]
+
+    def _poll(self):
+        while not self.stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index),
+                                      f"--query-gpu={self.QUERY}",
+                                      "--format=csv,noheader,nounits"],
+                                     capture_output=True, text=True, timeout=5).stdout
+                parts = [p.strip() for p in out.strip().split(",")]
+                sm, mx = float(parts[0]), float(parts[1])
+                reasons = {n for n, v in zip(self.NAMES, parts[3:7]) if v.lower() == "active"}
+                self.samples.append((time.perf_counter(), sm, mx, reasons))
+            except Exception:
+                time.sleep(0.05)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except Exception:
-            self.proc = None
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def mark(self, which: int):
+        self.window[which] = time.perf_counter()
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        self.stop.set()
+        self.thread.join(timeout=10)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        t0, t1 = self.window
+        inside = [s for s in self.samples if t0 is not None and t0 <= s[0] <= t1]
+        note = "inside timed region"
+        if not inside and self.samples and t0 is not None:
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(self.samples, key=lambda s: abs(s[0] - mid))[:3]
+            note = "timed region shorter than one poll; nearest samples"
+        sm = [s[1] for s in inside]
+        reasons = sorted(set().union(*[s[3] for s in inside])) if inside else []
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": inside[0][2] if inside else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
 
 
 def traffic_record(kernel_key: str):
@@ -224,6 +228,7 @@ def run_gpu(args, w):
         if dist is not None:
             dist.barrier()
 
+    clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         s.step()
     torch.cuda.synchronize()
@@ -233,15 +238,17 @@ def run_gpu(args, w):
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            s.flush.zero_()
-            ev[i][0].record(stream)
-            s.write()
-            ev[i][1].record(stream)
-            s.decode()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
+    clk.mark(0)
+    for i in range(args.steps):
+        s.flush.zero_()
+        ev[i][0].record(stream)
+        s.write()
+        ev[i][1].record(stream)
+        s.decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clk.mark(1)
+    clk.__exit__(None, None, None)
     barrier()
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
@@ -400,8 +407,8 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -58,6 +58,20 @@ __device__ __forceinline__ int phys_of_logical(int k, bool typeB) {
   return typeB ? 16 * j + i + 8 * e : 16 * j + 8 * (i >> 2) + (i & 3) + 4 * e;
 }
 
+// Inverse of phys_of_logical.
+__device__ __forceinline__ int logical_of_phys(int p, bool typeB) {
+  const int j = p >> 4, rem = p & 15;
+  int i, e;
+  if (typeB) {
+    e = rem >> 3;
+    i = rem & 7;
+  } else {
+    e = (rem >> 2) & 1;
+    i = 4 * (rem >> 3) + (rem & 3);
+  }
+  return 16 * (i >> 1) + 8 * (i & 1) + 2 * j + e;
+}
+
 // Physical channel of PV output column n (0..7) of tile chunk c (0..7).
 __device__ __forceinline__ int phys_of_chunk(int c, int n, bool typeB) {
   const int jj = c >> 1, wd = c & 1, r = n >> 1, e = n & 1, i = 4 * wd + r;
@@ -72,26 +86,34 @@ __device__ __forceinline__ uint32_t h2fma(uint32_t x, uint32_t m, uint32_t a) {
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16 1024 in both halves
 
-// 8 nibbles (channels 0..7 of the word) -> (c0,c4) (c1,c5) (c2,c6) (c3,c7).
+// Codes are centred before they reach the tensor cores (INT4: c - 8 in
+// [-8, 7]; INT2: c - 2 in [-2, 1]) and the min is moved by the same amount
+// (m' = m + 8s or m + 2s).  The products stay exact; the point is that the MMA
+// sums over thousands of tokens then have mixed signs, so the fp32 tensor-core
+// accumulation, whose adds are not round-to-nearest, does not drift.
+constexpr int kCentre4 = 8;
+constexpr int kCentre2 = 2;
+
+// 8 nibbles (channels 0..7 of the word) -> (c0,c4) (c1,c5) (c2,c6) (c3,c7), minus 8.
 __device__ __forceinline__ void unpack_int4(uint32_t w, uint32_t* p) {
   const uint32_t w8 = w >> 8;
-  p[0] = h2fma((w & 0x000F000Fu) | kMagic, 0x3C003C00u, 0xE400E400u);   // x*1 - 1024
-  p[1] = h2fma((w & 0x00F000F0u) | kMagic, 0x2C002C00u, 0xD400D400u);   // x/16 - 64
-  p[2] = h2fma((w8 & 0x000F000Fu) | kMagic, 0x3C003C00u, 0xE400E400u);
-  p[3] = h2fma((w8 & 0x00F000F0u) | kMagic, 0x2C002C00u, 0xD400D400u);
+  p[0] = h2fma((w & 0x000F000Fu) | kMagic, 0x3C003C00u, 0xE408E408u);   // x*1 - 1032
+  p[1] = h2fma((w & 0x00F000F0u) | kMagic, 0x2C002C00u, 0xD480D480u);   // x/16 - 72
+  p[2] = h2fma((w8 & 0x000F000Fu) | kMagic, 0x3C003C00u, 0xE408E408u);
+  p[3] = h2fma((w8 & 0x00F000F0u) | kMagic, 0x2C002C00u, 0xD480D480u);
 }
 
-// 16 crumbs (channels 0..15) -> (c0,c8) (c1,c9) ... (c7,c15).
+// 16 crumbs (channels 0..15) -> (c0,c8) (c1,c9) ... (c7,c15), minus 2.
 __device__ __forceinline__ void unpack_int2(uint32_t w, uint32_t* p) {
   const uint32_t w8 = w >> 8;
-  p[0] = h2fma((w & 0x00030003u) | kMagic, 0x3C003C00u, 0xE400E400u);   // x - 1024
-  p[1] = h2fma((w & 0x000C000Cu) | kMagic, 0x34003400u, 0xDC00DC00u);   // x/4 - 256
-  p[2] = h2fma((w & 0x00300030u) | kMagic, 0x2C002C00u, 0xD400D400u);   // x/16 - 64
-  p[3] = h2fma((w & 0x00C000C0u) | kMagic, 0x24002400u, 0xCC00CC00u);   // x/64 - 16
-  p[4] = h2fma((w8 & 0x00030003u) | kMagic, 0x3C003C00u, 0xE400E400u);
-  p[5] = h2fma((w8 & 0x000C000Cu) | kMagic, 0x34003400u, 0xDC00DC00u);
-  p[6] = h2fma((w8 & 0x00300030u) | kMagic, 0x2C002C00u, 0xD400D400u);
-  p[7] = h2fma((w8 & 0x00C000C0u) | kMagic, 0x24002400u, 0xCC00CC00u);
+  p[0] = h2fma((w & 0x00030003u) | kMagic, 0x3C003C00u, 0xE402E402u);   // x - 1026
+  p[1] = h2fma((w & 0x000C000Cu) | kMagic, 0x34003400u, 0xDC08DC08u);   // x/4 - 258
+  p[2] = h2fma((w & 0x00300030u) | kMagic, 0x2C002C00u, 0xD420D420u);   // x/16 - 66
+  p[3] = h2fma((w & 0x00C000C0u) | kMagic, 0x24002400u, 0xCC80CC80u);   // x/64 - 18
+  p[4] = h2fma((w8 & 0x00030003u) | kMagic, 0x3C003C00u, 0xE402E402u);
+  p[5] = h2fma((w8 & 0x000C000Cu) | kMagic, 0x34003400u, 0xDC08DC08u);
+  p[6] = h2fma((w8 & 0x00300030u) | kMagic, 0x2C002C00u, 0xD420D420u);
+  p[7] = h2fma((w8 & 0x00C000C0u) | kMagic, 0x24002400u, 0xCC80CC80u);
 }
 
 // 16 bf16 values (v[k] = channels 2k, 2k+1) -> fp16 pairs in the given pairing.
@@ -220,25 +242,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
     a.seq_split[2 * b + 1] = nsplit;
   }
 
-  // ---- stage q (fp16, permuted contraction order) and its group sums
+  // ---- stage q (fp16, permuted contraction order) and its group sums: thread
+  // t < 144 owns (group g, head h), loads its 64 values with 8 vector loads and
+  // sums them in a fixed order.
   {
-    const uint16_t* qg = a.q + ((long long)b * a.H + hc * kHC) * kDim;
-    for (int idx = tid; idx < kHC * kDim; idx += kThreads) {
-      const int h = idx / kDim, k = idx % kDim;
-      const int g = k >> 6;
-      const bool tb = g < 8 ? kTypeB : false;
-      const int phys = (g << 6) + phys_of_logical(k & 63, tb);
-      const float v = __uint_as_float(static_cast<uint32_t>(qg[h * kDim + phys]) << 16);
-      qs[h * kQStride + k] = __float2half_rn(v);
-    }
-    // zero the content tile: rows that are never written stay finite
     for (int idx = tid; idx < kPageTokens * kTileRow / 16; idx += kThreads)
       reinterpret_cast<uint4*>(tile)[idx] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
     if (tid < kGroups * kHC) {
       const int g = tid / kHC, h = tid % kHC;
+      const bool tb = g < 8 ? kTypeB : false;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((long long)b * a.H + hc * kHC + h) * kDim + g * 64);
+      uint4 v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) v[c] = src[c];
       float acc = 0.f;
-      for (int k = 0; k < 64; ++k) acc += __half2float(qs[h * kQStride + g * 64 + k]);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int p = c * 8 + e;
+          const float f = (e & 1) ? bf16hi_to_f32(w[e >> 1]) : bf16lo_to_f32(w[e >> 1]);
+          const __half hv = __float2half_rn(f);
+          acc += __half2float(hv);
+          qs[h * kQStride + g * 64 + logical_of_phys(p, tb)] = hv;
+        }
+      }
       qsum[g * kHC + h] = acc;
     }
     __syncthreads();
@@ -329,10 +359,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
             ldmatrix_x4(af, qs + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
             mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
           }
+          const float centre = (g < 8 && CB == 2) ? float(kCentre2) : float(kCentre4);
           const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(mt0[g])));
-          const float m0 = __half2float(__ushort_as_half(static_cast<unsigned short>(mt0[g] >> 16)));
           const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(mt1[g])));
-          const float m1 = __half2float(__ushort_as_half(static_cast<unsigned short>(mt1[g] >> 16)));
+          const float m0 = fmaf(centre, s0,
+              __half2float(__ushort_as_half(static_cast<unsigned short>(mt0[g] >> 16))));
+          const float m1 = fmaf(centre, s1,
+              __half2float(__ushort_as_half(static_cast<unsigned short>(mt1[g] >> 16))));
           const float q0 = qsum[g * kHC + h0], q1 = qsum[g * kHC + h0 + 8];
           S[0] += s0 * D[0] + m0 * q0;
           S[1] += s1 * D[1] + m1 * q0;
