@@ -587,39 +587,73 @@ struct CombineArgs {
   int B, H, total_splits;
 };
 
-__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+constexpr int kCombineThreads = 128;
+constexpr int kCombineMaxW = 1024;  // split weights kept in shared memory
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float t = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, t) : v + t;
+  }
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+  for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  return v;
+}
+
+// One block per (sequence, head): the split weights 2^(m_s - M) go to shared
+// memory once, then every thread sums its 4 channels over the splits with
+// independent (unrolled, branch-free) loads.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+  __shared__ float wsm[kCombineMaxW];
+  __shared__ float red[kCombineThreads / 32];
   const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
   int off = a.seq_split[2 * b], n = a.seq_split[2 * b + 1];
   off = min(max(off, 0), a.total_splits);
   n = min(max(n, 0), a.total_splits - off);
+  const float* ml = a.part_ml + ((long long)off * a.H + h) * 2;
+  const long long mstride = (long long)a.H * 2;
   float M = -INFINITY;
-  for (int s = 0; s < n; ++s) {
-    const float m = a.part_ml[((long long)(off + s) * a.H + h) * 2];
-    const float l = a.part_ml[((long long)(off + s) * a.H + h) * 2 + 1];
-    if (l > 0.f) M = fmaxf(M, m);
+  for (int s = threadIdx.x; s < n; s += kCombineThreads)
+    if (ml[s * mstride + 1] > 0.f) M = fmaxf(M, ml[s * mstride]);
+  M = block_reduce(M, true, red);
+  float den = 0.f;
+  for (int s = threadIdx.x; s < n; s += kCombineThreads) {
+    const float l = ml[s * mstride + 1];
+    const float w = l > 0.f ? fast_exp2(ml[s * mstride] - M) : 0.f;
+    den += w * l;
+    if (s < kCombineMaxW) wsm[s] = w;
   }
-  float denom = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  den = block_reduce(den, false, red);
   const int c = threadIdx.x * 4;
+  const float* o = a.part_o + ((long long)off * a.H + h) * kLatent + c;
+  const long long ostride = (long long)a.H * kLatent;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
   for (int s = 0; s < n; ++s) {
-    const long long base = (long long)(off + s) * a.H + h;
-    const float m = a.part_ml[base * 2];
-    const float l = a.part_ml[base * 2 + 1];
-    if (!(l > 0.f)) continue;
-    const float w = fast_exp2(m - M);
-    denom += w * l;
-    const float4 v = *reinterpret_cast<const float4*>(a.part_o + base * kLatent + c);
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
+    float w;
+    if (s < kCombineMaxW) {
+      w = wsm[s];
+    } else {
+      const float l = ml[s * mstride + 1];
+      w = l > 0.f ? fast_exp2(ml[s * mstride] - M) : 0.f;
+    }
+    const float4 v = *reinterpret_cast<const float4*>(o + s * ostride);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
-  const float inv = denom > 0.f ? 1.f / denom : 0.f;
-  float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  *reinterpret_cast<float4*>(a.out + ((long long)b * a.H + h) * kLatent + c) = r;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  *reinterpret_cast<float4*>(a.out + ((long long)b * a.H + h) * kLatent + c) =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   if (a.lse && threadIdx.x == 0)
-    a.lse[(long long)b * a.H + h] = denom > 0.f ? (M + log2f(denom)) * 0.69314718055994531f
-                                                 : -INFINITY;
+    a.lse[(long long)b * a.H + h] = den > 0.f ? (M + log2f(den)) * 0.69314718055994531f
+                                              : -INFINITY;
 }
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
@@ -648,7 +682,7 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
-  combine_kernel<<<a.B * a.H, 128, 0, stream>>>(ca);
+  combine_kernel<<<a.B * a.H, kCombineThreads, 0, stream>>>(ca);
   return cudaGetLastError();
 }
 
