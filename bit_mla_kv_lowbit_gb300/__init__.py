@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     LibraryError,
     bytes_per_token,
     decode,
+    decode_noalloc,
     decode_plan,
     layout,
     load,

@@ -25,6 +25,7 @@ EXPORTS = (
     "mla_lowbit_write",
     "mla_lowbit_decode_plan",
     "mla_lowbit_decode",
+    "mla_lowbit_decode_noalloc",
     "mla_lowbit_read_error",
     "mla_lowbit_strerror",
     "mla_lowbit_version",
@@ -77,6 +78,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_lowbit_decode.argtypes = [lp, i32, i32, ctypes.c_float, vp, vp, i64, vp, i32, vp, vp,
                                       vp, vp, vp, vp, vp, sz, vp, vp]
     lib.mla_lowbit_decode.restype = i32
+    lib.mla_lowbit_decode_noalloc.argtypes = [lp, i32, i32, ctypes.c_float, vp, vp, i64, vp, i32,
+                                              vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.mla_lowbit_decode_noalloc.restype = i32
     lib.mla_lowbit_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_lowbit_read_error.restype = i32
     lib.mla_lowbit_strerror.argtypes = [i32]
@@ -210,6 +214,40 @@ def decode(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink
         lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream))
     _check(st, "mla_lowbit_decode")
+
+
+def decode_noalloc(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink_buf,
+                   recent_buf, out, err_word, softmax_scale: float, lse=None, stream=None):
+    """mla_lowbit_decode_noalloc: the decode without a caller workspace.
+
+    For hosts that can hand the library only inputs and outputs (no device
+    allocation allowed); the split partials go to a fixed 32 MiB array the
+    library keeps on each device.  Calls that overlap on the GPU race on that
+    array, so keep them on one stream."""
+    torch = _torch()
+    B, H, _ = q.shape
+    _expect(q, "q", torch.bfloat16, (B, H, 576))
+    _expect(page_pool, "page_pool", torch.uint8)
+    _expect(block_table, "block_table", torch.int32)
+    _expect(seq_lens, "seq_lens", torch.int32, (B,))
+    _expect(out, "out", torch.float32, (B, H, 512))
+    _expect(err_word, "err_word", torch.int32, (1,))
+    if lse is not None:
+        _expect(lse, "lse", torch.float32, (B, H))
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    if lay.content_bits != 16:
+        _expect(sink_buf, "sink_buf", torch.bfloat16, (B, 4, 576))
+        _expect(recent_buf, "recent_buf", torch.bfloat16, (B, 128, 576))
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("seq_lens_host must have one entry per sequence")
+    st = load().mla_lowbit_decode_noalloc(
+        ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
+        page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
+        _ptr(lse), _ptr(err_word), _stream(stream))
+    _check(st, "mla_lowbit_decode_noalloc")
 
 
 def read_error(err_word) -> int:

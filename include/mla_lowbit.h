@@ -166,6 +166,34 @@ int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
                       void* workspace, size_t workspace_bytes, int32_t* err_word,
                       void* stream);
 
+/* mla_lowbit_decode for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this entry point: it exists because some hosts
+ * give a kernel only its inputs and outputs -- a serving engine that has
+ * already reserved almost all of HBM for its own cache pool, a plug-in
+ * interface without a workspace argument, or a loop that cannot afford the
+ * device-wide synchronisation of cudaMalloc.
+ *
+ * Same arguments, results and error handling as mla_lowbit_decode, minus the
+ * workspace: the split partials live in a fixed 32 MiB device array owned by
+ * the library (every GPU that loads the library holds it until the process
+ * exits).  Calls whose plan needs more than 32 MiB (see
+ * mla_lowbit_decode_plan) return MLA_LOWBIT_ESIZE and launch nothing.  The
+ * call allocates and frees nothing.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (nothing in it needs to start at zero: each call writes
+ * every byte it reads).  Calls that overlap on the GPU -- on different streams,
+ * or from different threads without ordering -- race on the array; issue them
+ * on one stream or order them yourself. */
+int mla_lowbit_decode_noalloc(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                              float softmax_scale, const void* q, const void* page_pool,
+                              int64_t num_pages, const int32_t* block_table, int max_pages,
+                              const int32_t* seq_lens, const int32_t* seq_lens_host,
+                              const void* sink_buf, const void* recent_buf, float* out,
+                              float* lse, int32_t* err_word, void* stream);
+
 /* Synchronously copies the device error word to *code_out (a blocking
  * cudaMemcpy: it waits for prior work on the legacy default stream). */
 int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out);
