@@ -11,7 +11,8 @@ namespace mlalb {
 namespace {
 
 constexpr int kMaxHeads = 128;
-constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSm = 1;
+constexpr long long kMaxChunkPages = 64;
 
 int check_layout(const mla_lowbit_layout* l) {
   if (!l) return MLA_LOWBIT_ENULL;
@@ -109,9 +110,16 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   }
   const long long head_chunks = heads / 16;
   const long long slots = (long long)num_sms * kCtasPerSm;
-  long long chunk = (work * head_chunks + slots - 1) / slots;
+  // packed layouts add one bf16 split per sequence: leave room for them in the
+  // same wave when there are few sequences
+  long long avail = slots - (packed ? (long long)num_seqs * head_chunks : 0);
+  if (avail < slots / 2) avail = slots / 2;
+  long long chunk = (work * head_chunks + avail - 1) / avail;
   if (chunk < 1) chunk = 1;
-  if (chunk > (1 << 20)) chunk = 1 << 20;
+  // a split accumulates at most kMaxChunkPages * 64 tokens in fp32 tensor-core
+  // accumulators (whose adds are not round-to-nearest); longer sequences get
+  // more splits, merged in fp32 by the combine kernel
+  if (chunk > kMaxChunkPages) chunk = kMaxChunkPages;
   long long total = 0;
   for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
   if (total > INT32_MAX / 2) return MLA_LOWBIT_ESIZE;

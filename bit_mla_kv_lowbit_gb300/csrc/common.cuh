@@ -140,5 +140,6 @@ struct DecodeArgs {
 cudaError_t launch_writer(int cbits, const WriterArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream);
+cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace mlalb

@@ -26,211 +26,89 @@
 // * The sink/recent bf16 tokens are one more split of the same sequence, so
 //   the combine kernel folds them into the one softmax.
 #include <cfloat>
+#include <cstdlib>
 
-#include "common.cuh"
+#include "decode_common.cuh"
 
 namespace mlalb {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kHC = 16;                 // heads per CTA
+constexpr int kTeams = 2;                 // independent 8-warp teams per CTA
+constexpr int kTeamWarps = 8;
+constexpr int kTeamThreads = kTeamWarps * 32;
+constexpr int kCtaWarps = kTeams * kTeamWarps;
+constexpr int kThreads = kCtaWarps * 32;
 constexpr int kTileRow = 1024;          // bytes per token row of the content tile
 constexpr int kQStride = kDim + 8;      // fp16 per q row in shared memory
 constexpr int kPStride = 72;            // floats per P row
-constexpr int kOffTile = 0;
-constexpr int kOffQ = kOffTile + kPageTokens * kTileRow;
-constexpr int kOffP = kOffQ + kHC * kQStride * 2;
-constexpr int kOffS = kOffP + kHC * kPStride * 4;
-constexpr int kOffM = kOffS + 8 * kPageTokens * 4;
-constexpr int kOffMax = kOffM + 8 * kPageTokens * 4;
-constexpr int kOffQsum = kOffMax + kWarps * kHC * 4;
+// shared by both teams
+constexpr int kOffQ = 0;
+constexpr int kOffQsum = kOffQ + kHC * kQStride * 2;
 constexpr int kOffScan = kOffQsum + kGroups * kHC * 4;
-constexpr int kSmemBytes = kOffScan + (kThreads + 64) * 4;
-
-// ---------------------------------------------------------------- pairing
-// The unpack of one thread's 16 channels (16j..16j+15 of a group) yields 8
-// fp16 pairs P_0..P_7.  INT4 ("type A"): P_i = (8(i>>2) + (i&3), +4).  INT2
-// ("type B"): P_i = (i, i+8).  mma k-step s takes b0 = P_2s, b1 = P_2s+1.
-
-__device__ __forceinline__ int phys_of_logical(int k, bool typeB) {
-  const int s = k >> 4, h = (k >> 3) & 1, j = (k >> 1) & 3, e = k & 1;
-  const int i = 2 * s + h;
-  return typeB ? 16 * j + i + 8 * e : 16 * j + 8 * (i >> 2) + (i & 3) + 4 * e;
+constexpr int kOffTeam = ((kOffScan + 64 * 4) + 127) / 128 * 128;
+// per team
+constexpr int kTOffTile = 0;
+constexpr int kTOffP = kTOffTile + kPageTokens * kTileRow;
+constexpr int kTOffS = kTOffP + kHC * kPStride * 4;
+constexpr int kTOffM = kTOffS + 8 * kPageTokens * 4;
+constexpr int kTOffMax = kTOffM + 8 * kPageTokens * 4;
+constexpr int kTOffStage = kTOffMax + kTeamWarps * kHC * 4;
+__host__ __device__ constexpr int team_bytes(int cbits) {
+  return kTOffStage + (cbits == 16 ? 0 : page_geom(cbits).page_bytes);
 }
-
-// Inverse of phys_of_logical.
-__device__ __forceinline__ int logical_of_phys(int p, bool typeB) {
-  const int j = p >> 4, rem = p & 15;
-  int i, e;
-  if (typeB) {
-    e = rem >> 3;
-    i = rem & 7;
-  } else {
-    e = (rem >> 2) & 1;
-    i = 4 * (rem >> 3) + (rem & 3);
-  }
-  return 16 * (i >> 1) + 8 * (i & 1) + 2 * j + e;
-}
-
-// Physical channel of PV output column n (0..7) of tile chunk c (0..7).
-__device__ __forceinline__ int phys_of_chunk(int c, int n, bool typeB) {
-  const int jj = c >> 1, wd = c & 1, r = n >> 1, e = n & 1, i = 4 * wd + r;
-  return typeB ? 16 * jj + i + 8 * e : 16 * jj + 8 * wd + r + 4 * e;
-}
-
-__device__ __forceinline__ uint32_t h2fma(uint32_t x, uint32_t m, uint32_t a) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&m),
-                      *reinterpret_cast<__half2*>(&a));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-constexpr uint32_t kMagic = 0x64006400u;  // fp16 1024 in both halves
-
-// Codes are centred before they reach the tensor cores (INT4: c - 8 in
-// [-8, 7]; INT2: c - 2 in [-2, 1]) and the min is moved by the same amount
-// (m' = m + 8s or m + 2s).  The products stay exact; the point is that the MMA
-// sums over thousands of tokens then have mixed signs, so the fp32 tensor-core
-// accumulation, whose adds are not round-to-nearest, does not drift.
-constexpr int kCentre4 = 8;
-constexpr int kCentre2 = 2;
-
-// 8 nibbles (channels 0..7 of the word) -> (c0,c4) (c1,c5) (c2,c6) (c3,c7), minus 8.
-__device__ __forceinline__ void unpack_int4(uint32_t w, uint32_t* p) {
-  const uint32_t w8 = w >> 8;
-  p[0] = h2fma((w & 0x000F000Fu) | kMagic, 0x3C003C00u, 0xE408E408u);   // x*1 - 1032
-  p[1] = h2fma((w & 0x00F000F0u) | kMagic, 0x2C002C00u, 0xD480D480u);   // x/16 - 72
-  p[2] = h2fma((w8 & 0x000F000Fu) | kMagic, 0x3C003C00u, 0xE408E408u);
-  p[3] = h2fma((w8 & 0x00F000F0u) | kMagic, 0x2C002C00u, 0xD480D480u);
-}
-
-// 16 crumbs (channels 0..15) -> (c0,c8) (c1,c9) ... (c7,c15), minus 2.
-__device__ __forceinline__ void unpack_int2(uint32_t w, uint32_t* p) {
-  const uint32_t w8 = w >> 8;
-  p[0] = h2fma((w & 0x00030003u) | kMagic, 0x3C003C00u, 0xE402E402u);   // x - 1026
-  p[1] = h2fma((w & 0x000C000Cu) | kMagic, 0x34003400u, 0xDC08DC08u);   // x/4 - 258
-  p[2] = h2fma((w & 0x00300030u) | kMagic, 0x2C002C00u, 0xD420D420u);   // x/16 - 66
-  p[3] = h2fma((w & 0x00C000C0u) | kMagic, 0x24002400u, 0xCC80CC80u);   // x/64 - 18
-  p[4] = h2fma((w8 & 0x00030003u) | kMagic, 0x3C003C00u, 0xE402E402u);
-  p[5] = h2fma((w8 & 0x000C000Cu) | kMagic, 0x34003400u, 0xDC08DC08u);
-  p[6] = h2fma((w8 & 0x00300030u) | kMagic, 0x2C002C00u, 0xD420D420u);
-  p[7] = h2fma((w8 & 0x00C000C0u) | kMagic, 0x24002400u, 0xCC80CC80u);
-}
-
-// 16 bf16 values (v[k] = channels 2k, 2k+1) -> fp16 pairs in the given pairing.
-template <bool kB>
-__device__ __forceinline__ void pairs_from_bf16(const uint32_t* v, uint32_t* p) {
-  float f[16];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    f[2 * k] = bf16lo_to_f32(v[k]);
-    f[2 * k + 1] = bf16hi_to_f32(v[k]);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int a = kB ? i : 8 * (i >> 2) + (i & 3);
-    const int b = kB ? i + 8 : a + 4;
-    p[i] = pack_half2(f[a], f[b]);
-  }
-}
-
-__device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = pack_half2(a - hf.x, b - hf.y);
-}
-
-// ---------------------------------------------------------------- plan lookup
-// Every CTA recomputes the per-sequence split counts (same integer formula as
-// the host) and finds which (sequence, split) its blockIdx.x names.
-__device__ void find_split(const DecodeArgs& a, bool packed, int* scan, int& b_out,
-                           int& split_out, int& nsplit_out) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (a.B + kThreads - 1) / kThreads;
-  const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
-  const int max_tok = a.max_pages * kPageTokens;
-  int local = 0;
-  for (int b = b0; b < b1; ++b) {
-    int L = a.seq_lens[b];
-    if (L < 0 || L > max_tok) L = 0;
-    local += splits_of(L, packed, a.chunk_pages);
-  }
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) scan[warp] = incl;
-  if (tid == 0) scan[kWarps] = -1;
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const int t = scan[w];
-      scan[w] = acc;
-      acc += t;
-    }
-    scan[kWarps + 1] = acc;  // device-side total
-  }
-  __syncthreads();
-  const int excl = scan[warp] + incl - local;
-  const int target = blockIdx.x;
-  if (target >= excl && target < excl + local) {
-    int acc = excl;
-    for (int b = b0; b < b1; ++b) {
-      int L = a.seq_lens[b];
-      if (L < 0 || L > max_tok) L = 0;
-      const int n = splits_of(L, packed, a.chunk_pages);
-      if (target < acc + n) {
-        scan[kWarps + 2] = b;
-        scan[kWarps + 3] = target - acc;
-        scan[kWarps + 4] = n;
-        scan[kWarps] = 1;
-        break;
-      }
-      acc += n;
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
-    if (scan[kWarps + 1] != a.total_splits) set_error(a.err, MLA_LOWBIT_DEV_PLAN);
-    for (int b = 0; b < a.B; ++b) {
-      const int L = a.seq_lens[b];
-      if (L < 0 || L > max_tok) set_error(a.err, MLA_LOWBIT_DEV_BAD_LEN);
-    }
-  }
-  if (scan[kWarps] == 1) {
-    b_out = scan[kWarps + 2];
-    split_out = scan[kWarps + 3];
-    nsplit_out = scan[kWarps + 4];
-  } else {
-    b_out = -1;
-  }
-}
+__host__ __device__ constexpr int smem_bytes(int cbits) { return kOffTeam + kTeams * team_bytes(cbits); }
+static_assert(smem_bytes(4) <= 227 * 1024, "shared memory budget");
 
 // ---------------------------------------------------------------- split kernel
+__device__ __forceinline__ void team_sync(int team) {
+  asm volatile("bar.sync %0, %1;" ::"r"(team + 1), "r"(kTeamThreads) : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// XOR applied to the 16-byte chunk index of content row r in the staging copy:
+// it spreads the rows a half-warp reads over all 32 banks.
 template <int CB>
-__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a) {
+__device__ __forceinline__ int stage_swizzle(int r) {
+  return CB == 4 ? ((r & 3) << 1) : (r & 3);
+}
+
+// One CTA per (split, 16-head chunk), one CTA per SM.  Two independent teams
+// of 8 warps take alternate pages of the split, each with its own running max,
+// sum and output, and merge at the end.  Packed pages are copied into a
+// per-team staging buffer with cp.async one page ahead.
+template <int CB>
+__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a) {
   constexpr bool kPacked = CB != 16;
   constexpr bool kTypeB = CB == 2;  // pairing of the content groups
   constexpr PageGeom G = page_geom(CB);
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* tile = smem + kOffTile;
   __half* qs = reinterpret_cast<__half*>(smem + kOffQ);
-  float* P = reinterpret_cast<float*>(smem + kOffP);
-  float* smS = reinterpret_cast<float*>(smem + kOffS);
-  float* smM = reinterpret_cast<float*>(smem + kOffM);
-  float* smax = reinterpret_cast<float*>(smem + kOffMax);
   float* qsum = reinterpret_cast<float*>(smem + kOffQsum);
   int* scan = reinterpret_cast<int*>(smem + kOffScan);
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int team = tid / kTeamThreads, ttid = tid % kTeamThreads, warp = ttid >> 5;
+  uint8_t* tbase = smem + kOffTeam + team * team_bytes(CB);
+  uint8_t* tile = tbase + kTOffTile;
+  float* P = reinterpret_cast<float*>(tbase + kTOffP);
+  float* smS = reinterpret_cast<float*>(tbase + kTOffS);
+  float* smM = reinterpret_cast<float*>(tbase + kTOffM);
+  float* smax = reinterpret_cast<float*>(tbase + kTOffMax);
+  uint8_t* stage = tbase + kTOffStage;
   const int j = lane & 3, rn = lane >> 2;
   const int h0 = rn;  // rows h0 and h0 + 8 of the 16-head chunk
 
   int b, split, nsplit;
-  find_split(a, kPacked, scan, b, split, nsplit);
+  find_split<kThreads>(a, kPacked, scan, b, split, nsplit);
   if (b < 0) return;
   const int hc = blockIdx.y;
   const int L = [&] {
@@ -242,11 +120,52 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
     a.seq_split[2 * b + 1] = nsplit;
   }
 
+  // ---- work of this split
+  const bool bf16_split = kPacked && split == nsplit - 1;
+  int n_tiles, page_begin = 0, n_sink = 0, rec_start = 0, n_tok = 0;
+  if (bf16_split) {
+    n_sink = min(L, kSink);
+    rec_start = max(kSink, L - kLocal);
+    n_tok = n_sink + max(0, L - rec_start);
+    n_tiles = (n_tok + kPageTokens - 1) / kPageTokens;
+  } else {
+    const int pages = packed_pages_of(L, kPacked);
+    page_begin = split * a.chunk_pages;
+    n_tiles = max(0, min(a.chunk_pages, pages - page_begin));
+  }
+  const int valid_lo = kPacked ? kSink : 0;
+  const int valid_hi = kPacked ? L - kLocal : L;  // packed-served tokens [lo, hi)
+  bool use_stage = false;
+  if constexpr (kPacked) use_stage = !bf16_split;
+
+  // Copy packed page `tile_i` of this split into the team's staging buffer.
+  auto stage_page = [&](int tile_i) {
+    if constexpr (kPacked) {
+      const int page_idx = page_begin + tile_i;
+      const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
+      if (page >= 0 && page < a.num_pages) {
+        const uint8_t* src = a.pool + page * G.page_bytes;
+        constexpr int kChunks = G.page_bytes / 16;
+        constexpr int kRowChunks = G.content_row / 16;
+        constexpr int kContentChunks = kPageTokens * kRowChunks;
+        for (int k = ttid; k < kChunks; k += kTeamThreads) {
+          int dst = k * 16;
+          if (k < kContentChunks) {
+            const int r = k / kRowChunks, c = k % kRowChunks;
+            dst = G.content_off + r * G.content_row + ((c ^ stage_swizzle<CB>(r)) << 4);
+          }
+          cp_async16(stage + dst, src + k * 16);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
   // ---- stage q (fp16, permuted contraction order) and its group sums: thread
   // t < 144 owns (group g, head h), loads its 64 values with 8 vector loads and
-  // sums them in a fixed order.
+  // sums them in a fixed order.  Each team zeroes its content tile.
   {
-    for (int idx = tid; idx < kPageTokens * kTileRow / 16; idx += kThreads)
+    for (int idx = ttid; idx < kPageTokens * kTileRow / 16; idx += kTeamThreads)
       reinterpret_cast<uint4*>(tile)[idx] = make_uint4(0, 0, 0, 0);
     if (tid < kGroups * kHC) {
       const int g = tid / kHC, h = tid % kHC;
@@ -271,24 +190,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
       }
       qsum[g * kHC + h] = acc;
     }
+    if (use_stage && team < n_tiles) stage_page(team);
     __syncthreads();
   }
-
-  // ---- work of this split
-  const bool bf16_split = kPacked && split == nsplit - 1;
-  int n_tiles, page_begin = 0, n_sink = 0, rec_start = 0, n_tok = 0;
-  if (bf16_split) {
-    n_sink = min(L, kSink);
-    rec_start = max(kSink, L - kLocal);
-    n_tok = n_sink + max(0, L - rec_start);
-    n_tiles = (n_tok + kPageTokens - 1) / kPageTokens;
-  } else {
-    const int pages = packed_pages_of(L, kPacked);
-    page_begin = split * a.chunk_pages;
-    n_tiles = max(0, min(a.chunk_pages, pages - page_begin));
-  }
-  const int valid_lo = kPacked ? kSink : 0;
-  const int valid_hi = kPacked ? L - kLocal : L;  // packed-served tokens [lo, hi)
 
   float O[8][4];
 #pragma unroll
@@ -296,101 +200,98 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
   float m_run0 = -INFINITY, m_run1 = -INFINITY;
   float accm0 = 0.f, accm1 = 0.f, l0 = 0.f, l1 = 0.f;
 
-  const int rowB = warp * 8 + rn;   // tile row of this thread's B fragment
+  const int rowB = warp * 8 + rn;    // tile row of this thread's B fragment
   const int tC0 = warp * 8 + 2 * j;  // tile rows of this thread's C columns
 
-  for (int tile_i = 0; tile_i < n_tiles; ++tile_i) {
+  for (int tile_i = team; tile_i < n_tiles; tile_i += kTeams) {
+    if (use_stage) cp_async_wait_all();
+    team_sync(team);
     // ================= phase 1: unpack + QK for tokens 8w..8w+7
     float S[4] = {0.f, 0.f, 0.f, 0.f};
     bool v0, v1;  // validity of tokens tC0, tC0+1
-    bool use_packed = false;
-    if constexpr (kPacked) use_packed = !bf16_split;
-    if (use_packed) {
+    if (use_stage) {
       if constexpr (kPacked) {
-      const int page_idx = page_begin + tile_i;
-      const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
-      const bool page_ok = page >= 0 && page < a.num_pages;
-      if (!page_ok && tid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
-      const int tok0 = page_idx * kPageTokens;
-      v0 = page_ok && tok0 + tC0 >= valid_lo && tok0 + tC0 < valid_hi;
-      v1 = page_ok && tok0 + tC0 + 1 >= valid_lo && tok0 + tC0 + 1 < valid_hi;
-      if (page_ok) {
-        const uint8_t* pb = a.pool + page * G.page_bytes;
-        uint32_t cw[kGroups][2];
+        const int page_idx = page_begin + tile_i;
+        const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
+        const bool page_ok = page >= 0 && page < a.num_pages;
+        if (!page_ok && ttid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+        const int tok0 = page_idx * kPageTokens;
+        v0 = page_ok && tok0 + tC0 >= valid_lo && tok0 + tC0 < valid_hi;
+        v1 = page_ok && tok0 + tC0 + 1 >= valid_lo && tok0 + tC0 + 1 < valid_hi;
+        if (page_ok) {
+          const uint8_t* sb = stage;
+          const int sw = stage_swizzle<CB>(rowB);
+          uint32_t cw[kGroups][2];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          if constexpr (CB == 4) {
-            const uint2 t = *reinterpret_cast<const uint2*>(pb + G.content_off +
-                                                             rowB * G.content_row + g * 32 + j * 8);
-            cw[g][0] = t.x;
-            cw[g][1] = t.y;
-          } else {
-            cw[g][0] = *reinterpret_cast<const uint32_t*>(pb + G.content_off +
-                                                          rowB * G.content_row + g * 16 + j * 4);
-            cw[g][1] = 0;
-          }
-        }
-        {
-          const uint2 t =
-              *reinterpret_cast<const uint2*>(pb + G.rope_off + rowB * G.rope_row + j * 8);
-          cw[8][0] = t.x;
-          cw[8][1] = t.y;
-        }
-        uint32_t mt0[kGroups], mt1[kGroups];
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          mt0[g] = *reinterpret_cast<const uint32_t*>(pb + G.meta_off + tC0 * G.meta_row + g * 4);
-          mt1[g] =
-              *reinterpret_cast<const uint32_t*>(pb + G.meta_off + (tC0 + 1) * G.meta_row + g * 4);
-        }
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          uint32_t bq[8];
-          if (g < 8 && CB == 2) {
-            unpack_int2(cw[g][0], bq);
-          } else {
-            unpack_int4(cw[g][0], bq);
-            unpack_int4(cw[g][1], bq + 4);
-          }
-          float D[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            uint32_t af[4];
-            ldmatrix_x4(af, qs + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
-            mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
-          }
-          const float centre = (g < 8 && CB == 2) ? float(kCentre2) : float(kCentre4);
-          const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(mt0[g])));
-          const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(mt1[g])));
-          const float m0 = fmaf(centre, s0,
-              __half2float(__ushort_as_half(static_cast<unsigned short>(mt0[g] >> 16))));
-          const float m1 = fmaf(centre, s1,
-              __half2float(__ushort_as_half(static_cast<unsigned short>(mt1[g] >> 16))));
-          const float q0 = qsum[g * kHC + h0], q1 = qsum[g * kHC + h0 + 8];
-          S[0] += s0 * D[0] + m0 * q0;
-          S[1] += s1 * D[1] + m1 * q0;
-          S[2] += s0 * D[2] + m0 * q1;
-          S[3] += s1 * D[3] + m1 * q1;
-          if (g < 8) {
-            uint8_t* rowp = tile + rowB * kTileRow;
-            const int c0 = (8 * g + 2 * j) ^ (rowB & 7), c1 = (8 * g + 2 * j + 1) ^ (rowB & 7);
-            *reinterpret_cast<uint4*>(rowp + c0 * 16) = make_uint4(bq[0], bq[1], bq[2], bq[3]);
-            *reinterpret_cast<uint4*>(rowp + c1 * 16) = make_uint4(bq[4], bq[5], bq[6], bq[7]);
-            if (rn == 0) {
-              smS[g * kPageTokens + tC0] = v0 ? s0 : 0.f;
-              smS[g * kPageTokens + tC0 + 1] = v1 ? s1 : 0.f;
-              smM[g * kPageTokens + tC0] = v0 ? m0 : 0.f;
-              smM[g * kPageTokens + tC0 + 1] = v1 ? m1 : 0.f;
+          for (int g = 0; g < 8; ++g) {
+            if constexpr (CB == 4) {
+              const int c = 2 * g + (j >> 1);
+              const uint2 t = *reinterpret_cast<const uint2*>(
+                  sb + G.content_off + rowB * G.content_row + ((c ^ sw) << 4) + 8 * (j & 1));
+              cw[g][0] = t.x;
+              cw[g][1] = t.y;
+            } else {
+              cw[g][0] = *reinterpret_cast<const uint32_t*>(
+                  sb + G.content_off + rowB * G.content_row + ((g ^ sw) << 4) + 4 * j);
+              cw[g][1] = 0;
             }
           }
-        }
-      } else if (rn == 0) {
+          {
+            const uint2 t =
+                *reinterpret_cast<const uint2*>(sb + G.rope_off + rowB * G.rope_row + j * 8);
+            cw[8][0] = t.x;
+            cw[8][1] = t.y;
+          }
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          smS[g * kPageTokens + tC0] = smS[g * kPageTokens + tC0 + 1] = 0.f;
-          smM[g * kPageTokens + tC0] = smM[g * kPageTokens + tC0 + 1] = 0.f;
+          for (int g = 0; g < kGroups; ++g) {
+            const uint32_t mt0 =
+                *reinterpret_cast<const uint32_t*>(sb + G.meta_off + tC0 * G.meta_row + g * 4);
+            const uint32_t mt1 =
+                *reinterpret_cast<const uint32_t*>(sb + G.meta_off + (tC0 + 1) * G.meta_row + g * 4);
+            uint32_t bq[8];
+            if (g < 8 && CB == 2) {
+              unpack_int2(cw[g][0], bq);
+            } else {
+              unpack_int4(cw[g][0], bq);
+              unpack_int4(cw[g][1], bq + 4);
+            }
+            float D[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              uint32_t af[4];
+              ldmatrix_x4(af, qs + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
+              mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
+            }
+            const float centre = (g < 8 && CB == 2) ? float(kCentre2) : float(kCentre4);
+            const float2 sm0 = __half22float2(*reinterpret_cast<const __half2*>(&mt0));
+            const float2 sm1 = __half22float2(*reinterpret_cast<const __half2*>(&mt1));
+            const float s0 = sm0.x, s1 = sm1.x;
+            const float m0 = fmaf(centre, s0, sm0.y), m1 = fmaf(centre, s1, sm1.y);
+            const float q0 = qsum[g * kHC + h0], q1 = qsum[g * kHC + h0 + 8];
+            S[0] += s0 * D[0] + m0 * q0;
+            S[1] += s1 * D[1] + m1 * q0;
+            S[2] += s0 * D[2] + m0 * q1;
+            S[3] += s1 * D[3] + m1 * q1;
+            if (g < 8) {
+              uint8_t* rowp = tile + rowB * kTileRow;
+              const int c0 = (8 * g + 2 * j) ^ (rowB & 7), c1 = (8 * g + 2 * j + 1) ^ (rowB & 7);
+              *reinterpret_cast<uint4*>(rowp + c0 * 16) = make_uint4(bq[0], bq[1], bq[2], bq[3]);
+              *reinterpret_cast<uint4*>(rowp + c1 * 16) = make_uint4(bq[4], bq[5], bq[6], bq[7]);
+              if (rn == 0) {
+                *reinterpret_cast<float2*>(&smS[g * kPageTokens + tC0]) =
+                    make_float2(v0 ? s0 : 0.f, v1 ? s1 : 0.f);
+                *reinterpret_cast<float2*>(&smM[g * kPageTokens + tC0]) =
+                    make_float2(v0 ? m0 : 0.f, v1 ? m1 : 0.f);
+              }
+            }
+          }
+        } else if (rn == 0) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            *reinterpret_cast<float2*>(&smS[g * kPageTokens + tC0]) = make_float2(0.f, 0.f);
+            *reinterpret_cast<float2*>(&smM[g * kPageTokens + tC0]) = make_float2(0.f, 0.f);
+          }
         }
-      }
       }
     } else {
       // bf16 rows: protected tokens of a packed cache, or bf16 pages.
@@ -408,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
         const int page_idx = page_begin + tile_i;
         const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
         const bool page_ok = page >= 0 && page < a.num_pages;
-        if (!page_ok && tid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+        if (!page_ok && ttid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
         const int tok0 = page_idx * kPageTokens;
         if (page_ok)
           rowptr = reinterpret_cast<const uint16_t*>(a.pool + page * G.page_bytes) + rowB * kDim;
@@ -446,10 +347,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
           *reinterpret_cast<uint4*>(rowp + c0 * 16) = make_uint4(bq[0], bq[1], bq[2], bq[3]);
           *reinterpret_cast<uint4*>(rowp + c1 * 16) = make_uint4(bq[4], bq[5], bq[6], bq[7]);
           if (rn == 0) {
-            smS[g * kPageTokens + tC0] = v0 ? 1.f : 0.f;
-            smS[g * kPageTokens + tC0 + 1] = v1 ? 1.f : 0.f;
-            smM[g * kPageTokens + tC0] = 0.f;
-            smM[g * kPageTokens + tC0 + 1] = 0.f;
+            *reinterpret_cast<float2*>(&smS[g * kPageTokens + tC0]) =
+                make_float2(v0 ? 1.f : 0.f, v1 ? 1.f : 0.f);
+            *reinterpret_cast<float2*>(&smM[g * kPageTokens + tC0]) = make_float2(0.f, 0.f);
           }
         }
       }
@@ -470,10 +370,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
       smax[warp * kHC + h0] = mx0;
       smax[warp * kHC + h0 + 8] = mx1;
     }
-    __syncthreads();
+    team_sync(team);
+    // the staging buffer is free again: fetch this team's next page
+    if (use_stage && tile_i + kTeams < n_tiles) stage_page(tile_i + kTeams);
     float t0 = -INFINITY, t1 = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kTeamWarps; ++w) {
       t0 = fmaxf(t0, smax[w * kHC + h0]);
       t1 = fmaxf(t1, smax[w * kHC + h0 + 8]);
     }
@@ -490,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
       *reinterpret_cast<float2*>(&P[h0 * kPStride + tC0]) = make_float2(p0, p1);
       *reinterpret_cast<float2*>(&P[(h0 + 8) * kPStride + tC0]) = make_float2(p2, p3);
     }
-    __syncthreads();
+    team_sync(team);
 
     // ================= phase 2: PV for content group g = warp
     {
@@ -546,16 +448,53 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
         }
       }
     }
-    __syncthreads();
   }
 
-  // ---- epilogue: finish the min term, write the partial (O, max, sum)
+  // ---- epilogue: finish the min term, merge the two teams, write the partial
 #pragma unroll
   for (int o = 1; o < 4; o <<= 1) {
     accm0 += __shfl_xor_sync(0xffffffffu, accm0, o);
     accm1 += __shfl_xor_sync(0xffffffffu, accm1, o);
     l0 += __shfl_xor_sync(0xffffffffu, l0, o);
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    O[c][0] += accm0;
+    O[c][1] += accm0;
+    O[c][2] += accm1;
+    O[c][3] += accm1;
+  }
+  // team 1 hands its state to team 0 through team 1's content tile
+  float* xch = reinterpret_cast<float*>(smem + kOffTeam + team_bytes(CB) + kTOffTile) + ttid * 36;
+  __syncthreads();
+  if (team == 1) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(xch + 4 * c) = make_float4(O[c][0], O[c][1], O[c][2], O[c][3]);
+    *reinterpret_cast<float4*>(xch + 32) = make_float4(m_run0, m_run1, l0, l1);
+  }
+  __syncthreads();
+  if (team == 1) return;
+  {
+    const float4 ml = *reinterpret_cast<const float4*>(xch + 32);
+    const float M0 = fmaxf(m_run0, ml.x), M1 = fmaxf(m_run1, ml.y);
+    const float a0 = M0 == -INFINITY ? 0.f : fast_exp2(m_run0 - M0);
+    const float b0 = M0 == -INFINITY ? 0.f : fast_exp2(ml.x - M0);
+    const float a1 = M1 == -INFINITY ? 0.f : fast_exp2(m_run1 - M1);
+    const float b1 = M1 == -INFINITY ? 0.f : fast_exp2(ml.y - M1);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 o = *reinterpret_cast<const float4*>(xch + 4 * c);
+      O[c][0] = a0 * O[c][0] + b0 * o.x;
+      O[c][1] = a0 * O[c][1] + b0 * o.y;
+      O[c][2] = a1 * O[c][2] + b1 * o.z;
+      O[c][3] = a1 * O[c][3] + b1 * o.w;
+    }
+    m_run0 = M0;
+    m_run1 = M1;
+    l0 = a0 * l0 + b0 * ml.z;
+    l1 = a1 * l1 + b1 * ml.w;
   }
   const int g = warp;
   const long long sidx = blockIdx.x;
@@ -564,10 +503,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
   float* o1 = a.part_o + (sidx * a.H + hg1) * kLatent + g * 64;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    o0[phys_of_chunk(c, 2 * j, kTypeB)] = O[c][0] + accm0;
-    o0[phys_of_chunk(c, 2 * j + 1, kTypeB)] = O[c][1] + accm0;
-    o1[phys_of_chunk(c, 2 * j, kTypeB)] = O[c][2] + accm1;
-    o1[phys_of_chunk(c, 2 * j + 1, kTypeB)] = O[c][3] + accm1;
+    o0[phys_of_chunk(c, 2 * j, kTypeB)] = O[c][0];
+    o0[phys_of_chunk(c, 2 * j + 1, kTypeB)] = O[c][1];
+    o1[phys_of_chunk(c, 2 * j, kTypeB)] = O[c][2];
+    o1[phys_of_chunk(c, 2 * j + 1, kTypeB)] = O[c][3];
   }
   if (warp == 0 && j == 0) {
     a.part_ml[(sidx * a.H + hg0) * 2] = m_run0;
@@ -656,28 +595,43 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
                                               : -INFINITY;
 }
 
+// Every layout runs on the mma.sync kernel above unless MLA_LOWBIT_DECODE=tc
+// selects the tcgen05 kernel (decode_tc.cu) for packed layouts.
+static bool use_mma_kernel(int cbits) {
+  if (cbits == 16) return true;
+  const char* v = getenv("MLA_LOWBIT_DECODE");
+  return !(v && v[0] == 't');
+}
+
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream) {
+  if (!use_mma_kernel(cbits)) {
+    cudaError_t et = launch_decode_tc(cbits, a, stream);
+    if (et != cudaSuccess) return et;
+    CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
+    combine_kernel<<<a.B * a.H, kCombineThreads, 0, stream>>>(ca);
+    return cudaGetLastError();
+  }
   static bool configured[3] = {false, false, false};
   const int k = cbits == 4 ? 0 : cbits == 2 ? 1 : 2;
   cudaError_t e = cudaSuccess;
   if (!configured[k]) {
     switch (cbits) {
       case 4: e = cudaFuncSetAttribute(decode_split_kernel<4>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); break;
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(4)); break;
       case 2: e = cudaFuncSetAttribute(decode_split_kernel<2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); break;
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2)); break;
       default: e = cudaFuncSetAttribute(decode_split_kernel<16>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(16));
     }
     if (e != cudaSuccess) return e;
     configured[k] = true;
   }
   dim3 grid(a.total_splits, a.H / kHC), block(kThreads);
   switch (cbits) {
-    case 4: decode_split_kernel<4><<<grid, block, kSmemBytes, stream>>>(a); break;
-    case 2: decode_split_kernel<2><<<grid, block, kSmemBytes, stream>>>(a); break;
-    default: decode_split_kernel<16><<<grid, block, kSmemBytes, stream>>>(a);
+    case 4: decode_split_kernel<4><<<grid, block, smem_bytes(4), stream>>>(a); break;
+    case 2: decode_split_kernel<2><<<grid, block, smem_bytes(2), stream>>>(a); break;
+    default: decode_split_kernel<16><<<grid, block, smem_bytes(16), stream>>>(a);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -74,7 +74,8 @@ enum {
   MLA_LOWBIT_DEV_BAD_POS = 2,   /* position < 0 or >= max_pages * 64 */
   MLA_LOWBIT_DEV_BAD_PAGE = 4,  /* block-table entry outside [0, num_pages) */
   MLA_LOWBIT_DEV_BAD_LEN = 8,   /* decode: seq_len < 0 or > max_pages * 64 */
-  MLA_LOWBIT_DEV_PLAN = 16      /* decode: device lengths disagree with seq_lens_host */
+  MLA_LOWBIT_DEV_PLAN = 16,     /* decode: device lengths disagree with seq_lens_host */
+  MLA_LOWBIT_DEV_TIMEOUT = 32   /* decode: an internal pipeline wait gave up (the output is invalid) */
 };
 
 /* Bytes of one 64-token page: 20736 (C4R4), 12544 (C2R4), 73728 (bf16).
@@ -126,7 +127,8 @@ int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* 
                      void* recent_buf, int32_t* err_word, void* stream);
 
 /* Split-KV plan of one decode call.  Pages of each sequence are cut into
- * splits of `chunk_pages` pages (chosen from the total work and the SM count);
+ * splits of `chunk_pages` pages (chosen from the total work and the SM count,
+ * at most 64 so that no split accumulates more than 4096 tokens);
  * packed layouts add one split per sequence for its bf16 tokens.  Writes the
  * number of splits and the workspace bytes the call needs.  num_sms == 0 asks
  * the current CUDA device. */
@@ -157,7 +159,11 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
  *   lse           [num_seqs][heads] float32, or NULL
  *   workspace     at least the bytes mla_lowbit_decode_plan reports
  *   err_word      int32 (device), OR-ed MLA_LOWBIT_DEV_* bits
- * Launches the split kernel and the log-sum-exp combine kernel on `stream`. */
+ * Launches the split kernel and the log-sum-exp combine kernel on `stream`.
+ * The split kernel runs on mma.sync tensor-core instructions; with the
+ * environment variable MLA_LOWBIT_DECODE=tc set at call time, packed layouts
+ * run on the tcgen05 (tensor-memory) kernel instead, with the same results
+ * within the stated tolerance. */
 int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
                       float softmax_scale, const void* q, const void* page_pool,
                       int64_t num_pages, const int32_t* block_table, int max_pages,
