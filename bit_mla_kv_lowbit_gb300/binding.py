@@ -31,7 +31,7 @@ EXPORTS = (
     "mla_lowbit_version",
 )
 
-DEV_BAD_SEQ, DEV_BAD_POS, DEV_BAD_PAGE, DEV_BAD_LEN, DEV_PLAN, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+DEV_BAD_SEQ, DEV_BAD_POS, DEV_BAD_PAGE, DEV_BAD_LEN, DEV_PLAN, DEV_PIPELINE = 1, 2, 4, 8, 16, 32
 
 
 class Layout(ctypes.Structure):

@@ -65,9 +65,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
+// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.  A pure
+// register operation (not volatile), so the compiler may interleave
+// independent accumulation chains.
 __device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -141,5 +143,6 @@ cudaError_t launch_writer(int cbits, const WriterArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream);
 cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_hy(int cbits, const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace mlalb

@@ -595,18 +595,25 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
                                               : -INFINITY;
 }
 
-// Every layout runs on the mma.sync kernel above unless MLA_LOWBIT_DECODE=tc
-// selects the tcgen05 kernel (decode_tc.cu) for packed layouts.
-static bool use_mma_kernel(int cbits) {
-  if (cbits == 16) return true;
+// Kernel for a layout: the mma.sync kernel above (the fastest measured on
+// GB300 for 16-head chunks) unless MLA_LOWBIT_DECODE selects, for packed
+// layouts, the hybrid mma.sync + tcgen05 kernel ("hy", decode_hy.cu) or the
+// all-tcgen05 kernel ("tc", decode_tc.cu).
+enum class SplitKernel { kMma, kHybrid, kTc };
+static SplitKernel split_kernel(int cbits) {
+  if (cbits == 16) return SplitKernel::kMma;
   const char* v = getenv("MLA_LOWBIT_DECODE");
-  return !(v && v[0] == 't');
+  if (v && v[0] == 'h') return SplitKernel::kHybrid;
+  if (v && v[0] == 't') return SplitKernel::kTc;
+  return SplitKernel::kMma;
 }
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream) {
-  if (!use_mma_kernel(cbits)) {
-    cudaError_t et = launch_decode_tc(cbits, a, stream);
+  const SplitKernel sk = split_kernel(cbits);
+  if (sk != SplitKernel::kMma) {
+    cudaError_t et = sk == SplitKernel::kTc ? launch_decode_tc(cbits, a, stream)
+                                            : launch_decode_hy(cbits, a, stream);
     if (et != cudaSuccess) return et;
     CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
     combine_kernel<<<a.B * a.H, kCombineThreads, 0, stream>>>(ca);

@@ -28,9 +28,10 @@
 //   warps 12-15 MMA issue (one lane each), and warp 12 owns the TMEM
 //               allocation.
 // Hand-offs use mbarriers; every wait is bounded and, if it gives up, the CTA
-// records MLA_LOWBIT_DEV_TIMEOUT, skips the remaining work and still frees its
+// records MLA_LOWBIT_DEV_PIPELINE, skips the remaining work and still frees its
 // tensor memory.
 #include "decode_common.cuh"
+#include "tc_util.cuh"
 
 namespace mlalb {
 namespace tc {
@@ -79,148 +80,6 @@ constexpr uint32_t kColQK = 0;     // 3 quads x 64
 constexpr uint32_t kColO = 192;    // 4 pairs x 64
 constexpr uint32_t kColM = 448;    // 64
 constexpr uint32_t kTmemCols = 512;
-
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
-
-__device__ __forceinline__ uint32_t su32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  // 128-byte swizzle, descriptor version 1
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ uint32_t idesc(int M, int N, int a_mn, int b_mn) {
-  // f16 x f16 -> f32
-  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(id), "r"(acc));
-}
-
-__device__ __forceinline__ void commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void bar_init(uint32_t bar, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void bar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Bounded wait on an mbarrier phase; on time-out raises the CTA abort flag.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                         int32_t* err) {
-  const long long t0 = clock64();
-  for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort = 1;
-      set_error(err, MLA_LOWBIT_DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-      "[%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                 "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// cp.async of 4, 8 or 16 bytes (global -> shared), one commit group per tile
-__device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes) {
-  const uint32_t d = su32(dst);
-  if (bytes == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-  else if (bytes == 8)
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// byte offset of fp16 element e (0..63) of row r inside a 128-byte-swizzled block
-__device__ __forceinline__ int sw_off(int r, int e) {
-  return (r >> 3) * 1024 + (r & 7) * 128 + ((((e >> 3) ^ (r & 7))) << 4) + (e & 7) * 2;
-}
-// byte offset of 16-byte chunk c of row r
-__device__ __forceinline__ int sw_chunk(int r, int c) {
-  return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-}
-
-// Physical channel (0..63 in its group) held at position e of logical chunk c of
-// a plane row, for the INT4 (type A) or INT2 (type B) unpack order.
-__device__ __forceinline__ int chan_of_pos(int c, int e, bool typeB) {
-  if (!typeB) return 8 * c + ((e & 1) ? 4 : 0) + (e >> 1);  // [0,4,1,5,2,6,3,7]
-  const int base = 16 * (c >> 1) + ((c & 1) ? 4 : 0);       // [0,8,1,9,..] / [4,12,5,13,..]
-  return base + ((e & 1) ? 8 : 0) + (e >> 1);
-}
 
 template <int CB>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
@@ -769,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
             : "memory");
         if (ok) break;
         if (clock64() - t0 > kWaitCycles) {
-          set_error(a.err, MLA_LOWBIT_DEV_TIMEOUT);
+          set_error(a.err, MLA_LOWBIT_DEV_PIPELINE);
           break;
         }
       }

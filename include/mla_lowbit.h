@@ -75,7 +75,8 @@ enum {
   MLA_LOWBIT_DEV_BAD_PAGE = 4,  /* block-table entry outside [0, num_pages) */
   MLA_LOWBIT_DEV_BAD_LEN = 8,   /* decode: seq_len < 0 or > max_pages * 64 */
   MLA_LOWBIT_DEV_PLAN = 16,     /* decode: device lengths disagree with seq_lens_host */
-  MLA_LOWBIT_DEV_TIMEOUT = 32   /* decode: an internal pipeline wait gave up (the output is invalid) */
+  MLA_LOWBIT_DEV_PIPELINE = 32  /* decode: an internal pipeline step failed -- a bounded wait gave up
+                                  or shared memory was misaligned (the output is invalid) */
 };
 
 /* Bytes of one 64-token page: 20736 (C4R4), 12544 (C2R4), 73728 (bf16).
@@ -160,10 +161,11 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
  *   workspace     at least the bytes mla_lowbit_decode_plan reports
  *   err_word      int32 (device), OR-ed MLA_LOWBIT_DEV_* bits
  * Launches the split kernel and the log-sum-exp combine kernel on `stream`.
- * The split kernel runs on mma.sync tensor-core instructions; with the
- * environment variable MLA_LOWBIT_DECODE=tc set at call time, packed layouts
- * run on the tcgen05 (tensor-memory) kernel instead, with the same results
- * within the stated tolerance. */
+ * The split kernel runs on mma.sync tensor-core instructions.  For packed
+ * layouts the environment variable MLA_LOWBIT_DECODE, read at call time,
+ * selects another split kernel with the same results within the stated
+ * tolerance: "hy" (QK on mma.sync, PV on tcgen05 with tensor-memory
+ * accumulators) or "tc" (QK and PV on tcgen05). */
 int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
                       float softmax_scale, const void* q, const void* page_pool,
                       int64_t num_pages, const int32_t* block_table, int max_pages,
