@@ -44,7 +44,8 @@ constexpr int kPStride = 72;            // floats per P row
 constexpr int kOffQ = 0;
 constexpr int kOffQsum = kOffQ + kHC * kQStride * 2;
 constexpr int kOffScan = kOffQsum + kGroups * kHC * 4;
-constexpr int kOffTeam = ((kOffScan + 64 * 4) + 127) / 128 * 128;
+constexpr int kOffPages = kOffScan + 64 * 4;  // [64] page ids of the split
+constexpr int kOffTeam = ((kOffPages + 64 * 4) + 127) / 128 * 128;
 // per team
 constexpr int kTOffTile = 0;
 constexpr int kTOffP = kTOffTile + kPageTokens * kTileRow;
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   float* smM = reinterpret_cast<float*>(tbase + kTOffM);
   float* smax = reinterpret_cast<float*>(tbase + kTOffMax);
   uint8_t* stage = tbase + kTOffStage;
+  int* s_pages = reinterpret_cast<int*>(smem + kOffPages);
   const int j = lane & 3, rn = lane >> 2;
   const int h0 = rn;  // rows h0 and h0 + 8 of the 16-head chunk
 
@@ -133,6 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     page_begin = split * a.chunk_pages;
     n_tiles = max(0, min(a.chunk_pages, pages - page_begin));
   }
+  if (n_tiles > 64) {  // the planner caps splits at 64 pages
+    if (tid == 0) set_error(a.err, MLA_LOWBIT_DEV_PLAN);
+    n_tiles = 0;
+  }
   const int valid_lo = kPacked ? kSink : 0;
   const int valid_hi = kPacked ? L - kLocal : L;  // packed-served tokens [lo, hi)
   bool use_stage = false;
@@ -141,8 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   // Copy packed page `tile_i` of this split into the team's staging buffer.
   auto stage_page = [&](int tile_i) {
     if constexpr (kPacked) {
-      const int page_idx = page_begin + tile_i;
-      const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
+      const long long page = s_pages[tile_i];
       if (page >= 0 && page < a.num_pages) {
         const uint8_t* src = a.pool + page * G.page_bytes;
         constexpr int kChunks = G.page_bytes / 16;
@@ -190,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       }
       qsum[g * kHC + h] = acc;
     }
+    if (kPacked && !bf16_split && tid < n_tiles && tid < 64)
+      s_pages[tid] = a.block_table[(long long)b * a.max_pages + page_begin + tid];
+    __syncthreads();  // page ids visible
     if (use_stage && team < n_tiles) stage_page(team);
     __syncthreads();
   }
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     if (use_stage) {
       if constexpr (kPacked) {
         const int page_idx = page_begin + tile_i;
-        const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
+        const long long page = s_pages[tile_i];
         const bool page_ok = page >= 0 && page < a.num_pages;
         if (!page_ok && ttid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
         const int tok0 = page_idx * kPageTokens;
