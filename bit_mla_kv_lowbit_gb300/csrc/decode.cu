@@ -522,6 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     a.part_ml[(sidx * a.H + hg1) * 2] = m_run1;
     a.part_ml[(sidx * a.H + hg1) * 2 + 1] = l1;
   }
+  // this CTA's partial is written: the combine may be launched
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- combine
@@ -534,61 +536,63 @@ struct CombineArgs {
   int B, H, total_splits;
 };
 
-constexpr int kCombineThreads = 128;
-constexpr int kCombineMaxW = 1024;  // split weights kept in shared memory
+constexpr int kCombineWarps = 2;  // 128-channel quarters per block
+constexpr int kCombineThreads = kCombineWarps * 32;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float t = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, t) : v + t;
-  }
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  v = red[0];
-  for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-  return v;
-}
-
-// One block per (sequence, head): the split weights 2^(m_s - M) go to shared
-// memory once, then every thread sums its 4 channels over the splits with
-// independent (unrolled, branch-free) loads.
+// One warp per (sequence, head, 128-channel quarter).  Lane s holds split s's
+// weight 2^(m_s - M) (splits beyond 32 recompute theirs); every lane then sums
+// its 4 channels over the splits with the weight broadcast by shuffle: no
+// shared memory and no block barrier.  Launched as a programmatic dependent
+// of the split kernel, it waits for the split kernel's results before reading
+// them.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
-  __shared__ float wsm[kCombineMaxW];
-  __shared__ float red[kCombineThreads / 32];
-  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (item >= a.B * a.H * 4) return;
+  const int quarter = item & 3, bh = item >> 2, b = bh / a.H, h = bh % a.H;
   int off = a.seq_split[2 * b], n = a.seq_split[2 * b + 1];
   off = min(max(off, 0), a.total_splits);
   n = min(max(n, 0), a.total_splits - off);
   const float* ml = a.part_ml + ((long long)off * a.H + h) * 2;
   const long long mstride = (long long)a.H * 2;
+  float m_mine = -INFINITY, l_mine = 0.f;  // split `lane`
   float M = -INFINITY;
-  for (int s = threadIdx.x; s < n; s += kCombineThreads)
-    if (ml[s * mstride + 1] > 0.f) M = fmaxf(M, ml[s * mstride]);
-  M = block_reduce(M, true, red);
-  float den = 0.f;
-  for (int s = threadIdx.x; s < n; s += kCombineThreads) {
-    const float l = ml[s * mstride + 1];
-    const float w = l > 0.f ? fast_exp2(ml[s * mstride] - M) : 0.f;
-    den += w * l;
-    if (s < kCombineMaxW) wsm[s] = w;
+  for (int s = lane; s < n; s += 32) {
+    const float2 v = *reinterpret_cast<const float2*>(ml + s * mstride);
+    if (s < 32) {
+      m_mine = v.x;
+      l_mine = v.y;
+    }
+    if (v.y > 0.f) M = fmaxf(M, v.x);
   }
-  den = block_reduce(den, false, red);
-  const int c = threadIdx.x * 4;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w_mine = (l_mine > 0.f && M != -INFINITY) ? fast_exp2(m_mine - M) : 0.f;
+  float den = w_mine * l_mine;
+  for (int s = lane + 32; s < n; s += 32) {
+    const float2 v = *reinterpret_cast<const float2*>(ml + s * mstride);
+    den += v.y > 0.f ? fast_exp2(v.x - M) * v.y : 0.f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const int c = quarter * 128 + lane * 4;
   const float* o = a.part_o + ((long long)off * a.H + h) * kLatent + c;
   const long long ostride = (long long)a.H * kLatent;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = 0; s < n; ++s) {
-    float w;
-    if (s < kCombineMaxW) {
-      w = wsm[s];
-    } else {
-      const float l = ml[s * mstride + 1];
-      w = l > 0.f ? fast_exp2(ml[s * mstride] - M) : 0.f;
-    }
+  const int n32 = min(n, 32);
+#pragma unroll 4
+  for (int s = 0; s < n32; ++s) {
+    const float w = __shfl_sync(0xffffffffu, w_mine, s);
+    const float4 v = *reinterpret_cast<const float4*>(o + s * ostride);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  for (int s = 32; s < n; ++s) {
+    const float2 mv = *reinterpret_cast<const float2*>(ml + s * mstride);
+    const float w = mv.y > 0.f ? fast_exp2(mv.x - M) : 0.f;
     const float4 v = *reinterpret_cast<const float4*>(o + s * ostride);
     acc.x = fmaf(w, v.x, acc.x);
     acc.y = fmaf(w, v.y, acc.y);
@@ -598,9 +602,27 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   const float inv = den > 0.f ? 1.f / den : 0.f;
   *reinterpret_cast<float4*>(a.out + ((long long)b * a.H + h) * kLatent + c) =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (a.lse && threadIdx.x == 0)
+  if (a.lse && quarter == 0 && lane == 0)
     a.lse[(long long)b * a.H + h] = den > 0.f ? (M + log2f(den)) * 0.69314718055994531f
                                               : -INFINITY;
+}
+
+// Launch the combine as a programmatic dependent of the kernel just queued on
+// `stream`, so that its launch overlaps the split kernel's last CTAs.
+static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
+  const int items = ca.B * ca.H * 4;
+  if (items == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((items + kCombineWarps - 1) / kCombineWarps);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, ca);
 }
 
 // Kernel for a layout: the mma.sync kernel above (the fastest measured on
@@ -624,8 +646,7 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
                                             : launch_decode_hy(cbits, a, stream);
     if (et != cudaSuccess) return et;
     CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
-    combine_kernel<<<a.B * a.H, kCombineThreads, 0, stream>>>(ca);
-    return cudaGetLastError();
+    return launch_combine(ca, stream);
   }
   static bool configured[3] = {false, false, false};
   const int k = cbits == 4 ? 0 : cbits == 2 ? 1 : 2;
@@ -651,8 +672,7 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
-  combine_kernel<<<a.B * a.H, kCombineThreads, 0, stream>>>(ca);
-  return cudaGetLastError();
+  return launch_combine(ca, stream);
 }
 
 }  // namespace mlalb

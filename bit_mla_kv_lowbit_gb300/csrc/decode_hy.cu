@@ -634,6 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
   // ---- teardown: the MMA warp has drained; free tensor memory
   tc_fence_before();
   __syncthreads();
+  // the partial of this CTA is written: the combine may be launched
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
