@@ -45,6 +45,28 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense fp16/bf16 tensor peak in TFLOP/s (the same rate for both types):
+    the measured burst figure, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def algorithmic_flops(w: syn.Workload, lens) -> float:
+    """Flops the decode must do per step: QK over 576 channels and PV over 512
+    for every cached token and head (2 flops per multiply-add)."""
+    return 2.0 * w.heads * (576 + 512) * float(np.sum(lens))
+
+
+def percentiles(xs, qs=(10, 50, 90)):
+    ys = sorted(xs)
+    return {f"p{q}": round(ys[min(len(ys) - 1, int(round(q / 100 * (len(ys) - 1))))], 5) for q in qs}
+
+
 def algorithmic_bytes(w: syn.Workload, lens) -> dict:
     """Bytes the decode must move per step, from the closed form: packed bytes of
     the packed-served tokens, bf16 bytes of the protected tokens, queries,
@@ -281,6 +303,9 @@ def run_gpu(args, w):
     by = algorithmic_bytes(w, s.lens)
     peak, peak_kind = peaks()
     dec_gbs = by["decode"] / (t_dec * 1e-3) / 1e9
+    tensor_bound = w.heads > 32 and w.content_bits != 16
+    tpk, tpk_kind = tensor_peak()
+    dec_tflops = algorithmic_flops(w, s.lens) / (t_dec * 1e-3) / 1e12
     trec = traffic_record(f"decode_{w.name}")
     n_launch_step = (1 if w.writer_in_step else 0) + 2
     if rank == 0:
@@ -307,13 +332,22 @@ def run_gpu(args, w):
             "hbm_frac": round(dec_gbs / peak, 4),
             "decode_us": round(t_dec * 1e3, 2),
             "kv_tokens_per_s": round(world * float(np.sum(s.lens)) / (t_step * 1e-3), 1),
-            "roofline": {"bound": "hbm" if w.heads <= 32 or w.content_bits == 16 else "tensor",
-                         "kernel": "decode (split + combine)",
-                         "achieved": round(dec_gbs, 1), "peak": peak,
-                         "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
-                         "frac": round(dec_gbs / peak, 4),
-                         "algorithmic_bytes": by["decode"],
-                         "traffic": (trec or {}).get("dram_bytes_per_launch")},
+            "roofline": ({"bound": "tensor", "kernel": "decode (split + combine)",
+                          "achieved": round(dec_tflops, 2), "peak": tpk,
+                          "peak_source": f"{tpk_kind} bf16_tflops (fp16 runs at the same rate)",
+                          "unit": "TFLOP/s", "frac": round(dec_tflops / tpk, 4),
+                          "algorithmic_flops": algorithmic_flops(w, s.lens),
+                          "hbm_frac": round(dec_gbs / peak, 4),
+                          "traffic": (trec or {}).get("dram_bytes_per_launch")}
+                         if tensor_bound else
+                         {"bound": "hbm", "kernel": "decode (split + combine)",
+                          "achieved": round(dec_gbs, 1), "peak": peak,
+                          "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                          "frac": round(dec_gbs / peak, 4),
+                          "algorithmic_bytes": by["decode"],
+                          "traffic": (trec or {}).get("dram_bytes_per_launch")}),
+            "step_ms_percentiles": percentiles(step_ms),
+            "decode_us_percentiles": {k: round(v * 1e3, 2) for k, v in percentiles(dec_ms).items()},
             "e2e": {"value": round(e2e_tokens_per_s, 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(s.h_q.numel() * 2 + (
                         (s.h_ckv.numel() + s.h_kr.numel()) * 2 if w.writer_in_step else 0)),
@@ -404,6 +438,79 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- context sweep
+
+TABLE9_CONTEXTS = (1024, 4096, 16384, 65536, 262144, 1048576)
+
+
+def run_table9(args):
+    """Decode latency against context length (QuantMLA, Table 9 caption and
+    Figure 5b: latency from 1K to 1M context at batch 8 and 32, C4R4 against
+    bf16 pages). One JSON line per (batch, context, layout); decode only (split
+    + combine), L2 flushed before each timed call. The caches are filled
+    through the library's writer from seeded device-generated tokens."""
+    import torch
+    import bit_mla_kv_lowbit_gb300 as pkg
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    heads = args.sweep_heads
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak, peak_kind = peaks()
+    chunk = 1 << 18
+    for B in (8, 32):
+        for L in TABLE9_CONTEXTS:
+            res = {}
+            for cb in (4, 16):
+                w = syn.custom(f"t9_b{B}_l{L}_c{cb}", [L] * B, heads=heads, content_bits=cb,
+                               rope_bits=4 if cb == 4 else 16, seed=9)
+                table, npages = syn.make_paging(w)
+                cache = pkg.PagedCache(cb, 4 if cb == 4 else 16, table, npages, dev)
+                lens_after = torch.full((B,), L, dtype=torch.int32, device=dev)
+                for b in range(B):
+                    for p0 in range(0, L, chunk):
+                        n = min(chunk, L - p0)
+                        ckv, kr = syn.device_tokens(n, seed=1000 * b + p0 // chunk, device=dev,
+                                                    start_pos=p0)
+                        cache.write(ckv, kr, torch.arange(p0, p0 + n, dtype=torch.int32, device=dev),
+                                    seq_idx=torch.full((n,), b, dtype=torch.int32, device=dev),
+                                    seq_lens_after=lens_after)
+                        del ckv, kr
+                g = torch.Generator(device=dev)
+                g.manual_seed(L + B)
+                q = torch.randn(B, heads, 576, generator=g, device=dev).to(torch.bfloat16)
+                out = torch.empty(B, heads, 512, dtype=torch.float32, device=dev)
+                lens_h = [L] * B
+                ws = cache.workspace(heads, lens_h)
+                for _ in range(3):
+                    cache.decode(q, lens_after, lens_h, w.softmax_scale, out=out, workspace=ws)
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(args.sweep_reps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    cache.decode(q, lens_after, lens_h, w.softmax_scale, out=out, workspace=ws)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+                assert cache.error() == 0, f"device error word {cache.error()}"
+                by = algorithmic_bytes(w, np.full(B, L))["decode"]
+                med = sorted(ts)[len(ts) // 2]
+                res[cb] = med
+                print(json.dumps({
+                    "sweep": "table9", "batch": B, "context": L, "heads": heads,
+                    "layout": "C4R4" if cb == 4 else "bf16",
+                    "decode_us": round(med, 2), **{k: round(v, 2) for k, v in
+                                                   percentiles(ts).items()},
+                    "algorithmic_bytes": by, "gbs": round(by / (med * 1e-6) / 1e9, 1),
+                    "hbm_frac": round(by / (med * 1e-6) / 1e9 / peak, 4),
+                    "peak_source": f"{peak_kind} hbm_gbs",
+                    "c4r4_vs_bf16_pct": (round(100.0 * (res[4] - med) / med, 1)
+                                         if cb == 16 else None)}), flush=True)
+                del cache, ws, out, q
+                torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -413,7 +520,14 @@ def main():
     ap.add_argument("--workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", choices=["table9"], default=None,
+                    help="context-length sweep instead of the benchmark line")
+    ap.add_argument("--sweep-heads", type=int, default=16)
+    ap.add_argument("--sweep-reps", type=int, default=15)
     args = ap.parse_args()
+    if args.sweep == "table9":
+        run_table9(args)
+        return
     w = syn.get(args.workload)
     if args.impl == "reference":
         run_reference(args, w)

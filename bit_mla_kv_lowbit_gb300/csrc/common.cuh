@@ -144,5 +144,6 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
                           cudaStream_t stream);
 cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_hy(int cbits, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_gw(int cbits, const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace mlalb

@@ -629,12 +629,13 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
 // GB300 for 16-head chunks) unless MLA_LOWBIT_DECODE selects, for packed
 // layouts, the hybrid mma.sync + tcgen05 kernel ("hy", decode_hy.cu) or the
 // all-tcgen05 kernel ("tc", decode_tc.cu).
-enum class SplitKernel { kMma, kHybrid, kTc };
+enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp };
 static SplitKernel split_kernel(int cbits) {
   if (cbits == 16) return SplitKernel::kMma;
   const char* v = getenv("MLA_LOWBIT_DECODE");
   if (v && v[0] == 'h') return SplitKernel::kHybrid;
   if (v && v[0] == 't') return SplitKernel::kTc;
+  if (v && v[0] == 'g') return SplitKernel::kGroupWarp;
   return SplitKernel::kMma;
 }
 
@@ -642,8 +643,9 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
                           cudaStream_t stream) {
   const SplitKernel sk = split_kernel(cbits);
   if (sk != SplitKernel::kMma) {
-    cudaError_t et = sk == SplitKernel::kTc ? launch_decode_tc(cbits, a, stream)
-                                            : launch_decode_hy(cbits, a, stream);
+    cudaError_t et = sk == SplitKernel::kTc     ? launch_decode_tc(cbits, a, stream)
+                     : sk == SplitKernel::kHybrid ? launch_decode_hy(cbits, a, stream)
+                                                  : launch_decode_gw(cbits, a, stream);
     if (et != cudaSuccess) return et;
     CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
     return launch_combine(ca, stream);

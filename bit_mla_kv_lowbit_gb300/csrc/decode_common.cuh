@@ -104,9 +104,10 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
 // ---------------------------------------------------------------- plan lookup
 // Every CTA recomputes the per-sequence split counts (same integer formula as
 // the host) and finds which (sequence, split) its blockIdx.x names.
+// `target` is the split's global index (blockIdx.x by default).
 template <int kThreads>
 __device__ void find_split(const DecodeArgs& a, bool packed, int* scan, int& b_out,
-                           int& split_out, int& nsplit_out) {
+                           int& split_out, int& nsplit_out, int target_index = -1) {
   constexpr int kCtaWarps = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (a.B + kThreads - 1) / kThreads;
@@ -138,7 +139,7 @@ __device__ void find_split(const DecodeArgs& a, bool packed, int* scan, int& b_o
   }
   __syncthreads();
   const int excl = scan[warp] + incl - local;
-  const int target = blockIdx.x;
+  const int target = target_index >= 0 ? target_index : (int)blockIdx.x;
   if (target >= excl && target < excl + local) {
     int acc = excl;
     for (int b = b0; b < b1; ++b) {

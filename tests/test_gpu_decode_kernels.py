@@ -1,7 +1,7 @@
 """The alternative split kernels vs the fp64 oracle: the hybrid mma.sync +
-tcgen05 kernel (MLA_LOWBIT_DECODE=hy) and the all-tcgen05 kernel
-(MLA_LOWBIT_DECODE=tc); the default (mma.sync) kernel is covered by
-test_gpu_decode.py.
+tcgen05 kernel (MLA_LOWBIT_DECODE=hy), the all-tcgen05 kernel
+(MLA_LOWBIT_DECODE=tc) and the group-per-warp kernel (MLA_LOWBIT_DECODE=gw);
+the default kernel is covered by test_gpu_decode.py.
 
 Same bar as the default kernel: max-abs error <= 2e-3 and rel-L2 <= 1e-3 per
 sequence; writer bytes bit-exact.
@@ -17,7 +17,7 @@ from workloads import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["hy", "tc"], autouse=True)
+@pytest.fixture(params=["hy", "tc", "gw"], autouse=True)
 def kernel(request, monkeypatch):
     monkeypatch.setenv("MLA_LOWBIT_DECODE", request.param)
     return request.param

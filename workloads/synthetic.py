@@ -209,3 +209,31 @@ def custom(name: str, lengths: Sequence[int], heads: int = 16, content_bits: int
     lengths = tuple(int(x) for x in lengths)
     return Workload(name, len(lengths), heads, "explicit", lengths, content_bits, rope_bits,
                     steps, seed)
+
+
+def device_tokens(n: int, seed: int, device, start_pos: int = 0):
+    """Seeded bf16 tokens generated on a torch device, for timing sweeps whose
+    sizes make host generation too slow (up to millions of tokens per
+    sequence).  Same recipe as ``sequence_tokens`` (lognormal(0, 0.5)
+    per-channel latent scales with 4 outlier channels x 10; N(0,1) RoPE pairs
+    rotated by ``pos * 10000**(-2i/64)``), drawn with torch's generator, so
+    the values differ from the host generator's.  Returns ``(ckv [n][512],
+    krope [n][64])`` as torch bf16 tensors.  Nothing checks these values
+    against the oracle; they only give the cache realistic statistics."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    scale = torch.exp(0.5 * torch.randn(LATENT, generator=g, device=device))
+    outliers = torch.randperm(LATENT, generator=g, device=device)[:4]
+    scale[outliers] *= 10.0
+    ckv = (torch.randn(n, LATENT, generator=g, device=device) * scale).to(torch.bfloat16)
+    ab = torch.randn(n, 2, ROPE // 2, generator=g, device=device)
+    pos = torch.arange(start_pos, start_pos + n, device=device, dtype=torch.float64)[:, None]
+    inv_freq = ROPE_THETA ** (-2.0 * torch.arange(ROPE // 2, device=device, dtype=torch.float64) / ROPE)
+    ang = pos * inv_freq[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)
+    a, b = ab[:, 0, :].double(), ab[:, 1, :].double()
+    rot = torch.empty(n, ROPE, device=device, dtype=torch.float32)
+    rot[:, 0::2] = (a * cos - b * sin).float()
+    rot[:, 1::2] = (a * sin + b * cos).float()
+    return ckv, rot.to(torch.bfloat16)
