@@ -210,17 +210,18 @@ class Setup:
         torch.cuda.synchronize()
         assert self.cache.error() == 0, "device error during prefill"
 
-    def write(self):
-        if self.w.writer_in_step:
-            self.cache.write(self.ckv, self.kr, self.pos, seq_lens_after=self.lens_d)
-
     def decode(self):
         self.cache.decode(self.q, self.lens_d, self.lens_h, self.w.softmax_scale, out=self.out,
                           workspace=self.ws)
 
     def step(self):
-        self.write()
-        self.decode()
+        """One decode step: with the writer in the step, the append of each
+        sequence's new token and the decode are one mla_lowbit_write_decode call."""
+        if self.w.writer_in_step:
+            self.cache.write_decode(self.ckv, self.kr, self.q, self.lens_d, self.lens_h,
+                                    self.w.softmax_scale, out=self.out, workspace=self.ws)
+        else:
+            self.decode()
 
     def step_e2e(self):
         """Same step through the public API from pinned host buffers."""
@@ -256,24 +257,22 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
 
     # ---- device-resident timed region: K steps, L2 flushed between them
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     clk.mark(0)
     for i in range(args.steps):
         s.flush.zero_()
         ev[i][0].record(stream)
-        s.write()
+        s.step()
         ev[i][1].record(stream)
-        s.decode()
-        ev[i][2].record(stream)
     torch.cuda.synchronize()
     clk.mark(1)
     clk.__exit__(None, None, None)
     barrier()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = step_ms  # the step is the (fused append +) decode call
 
     # ---- end to end through the public API with host buffers
     for _ in range(2):
@@ -302,12 +301,18 @@ def run_gpu(args, w):
     e2e_tokens_per_s = world * B / (t_e2e * 1e-3)
     by = algorithmic_bytes(w, s.lens)
     peak, peak_kind = peaks()
-    dec_gbs = by["decode"] / (t_dec * 1e-3) / 1e9
+    step_bytes = by["decode"] + by["writer"]
+    dec_gbs = step_bytes / (t_dec * 1e-3) / 1e9
     tensor_bound = w.heads > 32 and w.content_bits != 16
     tpk, tpk_kind = tensor_peak()
     dec_tflops = algorithmic_flops(w, s.lens) / (t_dec * 1e-3) / 1e12
     trec = traffic_record(f"decode_{w.name}")
-    n_launch_step = (1 if w.writer_in_step else 0) + 2
+    # split + combine; the append is fused into the default split kernel, the
+    # other kernels (MLA_LOWBIT_DECODE) run the writer kernel first
+    fused = w.writer_in_step and os.environ.get("MLA_LOWBIT_DECODE", "m")[:1] in ("", "m")
+    n_launch_step = 2 + (1 if w.writer_in_step and not fused else 0)
+    kernel_desc = ("append + decode (split kernel with fused append, combine)"
+                   if w.writer_in_step else "decode (split + combine)")
     if rank == 0:
         line = {
             "metric": METRIC,
@@ -332,7 +337,7 @@ def run_gpu(args, w):
             "hbm_frac": round(dec_gbs / peak, 4),
             "decode_us": round(t_dec * 1e3, 2),
             "kv_tokens_per_s": round(world * float(np.sum(s.lens)) / (t_step * 1e-3), 1),
-            "roofline": ({"bound": "tensor", "kernel": "decode (split + combine)",
+            "roofline": ({"bound": "tensor", "kernel": kernel_desc,
                           "achieved": round(dec_tflops, 2), "peak": tpk,
                           "peak_source": f"{tpk_kind} bf16_tflops (fp16 runs at the same rate)",
                           "unit": "TFLOP/s", "frac": round(dec_tflops / tpk, 4),
@@ -340,11 +345,11 @@ def run_gpu(args, w):
                           "hbm_frac": round(dec_gbs / peak, 4),
                           "traffic": (trec or {}).get("dram_bytes_per_launch")}
                          if tensor_bound else
-                         {"bound": "hbm", "kernel": "decode (split + combine)",
+                         {"bound": "hbm", "kernel": kernel_desc,
                           "achieved": round(dec_gbs, 1), "peak": peak,
                           "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                           "frac": round(dec_gbs / peak, 4),
-                          "algorithmic_bytes": by["decode"],
+                          "algorithmic_bytes": step_bytes,
                           "traffic": (trec or {}).get("dram_bytes_per_launch")}),
             "step_ms_percentiles": percentiles(step_ms),
             "decode_us_percentiles": {k: round(v * 1e3, 2) for k, v in percentiles(dec_ms).items()},

@@ -26,6 +26,7 @@ EXPORTS = (
     "mla_lowbit_decode_plan",
     "mla_lowbit_decode",
     "mla_lowbit_decode_noalloc",
+    "mla_lowbit_write_decode",
     "mla_lowbit_read_error",
     "mla_lowbit_strerror",
     "mla_lowbit_version",
@@ -81,6 +82,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_lowbit_decode_noalloc.argtypes = [lp, i32, i32, ctypes.c_float, vp, vp, i64, vp, i32,
                                               vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_lowbit_decode_noalloc.restype = i32
+    lib.mla_lowbit_write_decode.argtypes = [lp, i32, i32, ctypes.c_float, vp, vp, vp, vp, i64, vp,
+                                            i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.mla_lowbit_write_decode.restype = i32
     lib.mla_lowbit_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_lowbit_read_error.restype = i32
     lib.mla_lowbit_strerror.argtypes = [i32]
@@ -214,6 +218,41 @@ def decode(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink
         lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream))
     _check(st, "mla_lowbit_decode")
+
+
+def write_decode(lay: Layout, q, ckv_new, krope_new, page_pool, block_table, seq_lens,
+                 seq_lens_host, sink_buf, recent_buf, out, workspace, err_word,
+                 softmax_scale: float, lse=None, stream=None):
+    """mla_lowbit_write_decode: append one token per sequence (at position
+    seq_lens[s] - 1) and decode, in one call."""
+    torch = _torch()
+    B, H, _ = q.shape
+    _expect(q, "q", torch.bfloat16, (B, H, 576))
+    _expect(ckv_new, "ckv_new", torch.bfloat16, (B, 512))
+    _expect(krope_new, "krope_new", torch.bfloat16, (B, 64))
+    _expect(page_pool, "page_pool", torch.uint8)
+    _expect(block_table, "block_table", torch.int32)
+    _expect(seq_lens, "seq_lens", torch.int32, (B,))
+    _expect(out, "out", torch.float32, (B, H, 512))
+    _expect(workspace, "workspace", torch.uint8)
+    _expect(err_word, "err_word", torch.int32, (1,))
+    if lse is not None:
+        _expect(lse, "lse", torch.float32, (B, H))
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    if lay.content_bits != 16:
+        _expect(sink_buf, "sink_buf", torch.bfloat16, (B, 4, 576))
+        _expect(recent_buf, "recent_buf", torch.bfloat16, (B, 128, 576))
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("seq_lens_host must have one entry per sequence")
+    st = load().mla_lowbit_write_decode(
+        ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(ckv_new),
+        _ptr(krope_new), _ptr(page_pool), page_pool.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf),
+        _ptr(recent_buf), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _ptr(err_word), _stream(stream))
+    _check(st, "mla_lowbit_write_decode")
 
 
 def decode_noalloc(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink_buf,

@@ -60,6 +60,20 @@ class PagedCache:
                        stream=stream)
         return out
 
+    def write_decode(self, ckv_new, krope_new, q, seq_lens, seq_lens_host, softmax_scale: float,
+                     out=None, lse=None, workspace=None, stream=None):
+        """Append one token per sequence (at position seq_lens[s] - 1) and decode."""
+        torch = self.torch
+        B, H, _ = q.shape
+        if out is None:
+            out = torch.empty(B, H, 512, dtype=torch.float32, device=self.device)
+        if workspace is None:
+            workspace = self.workspace(H, seq_lens_host)
+        binding.write_decode(self.layout, q, ckv_new, krope_new, self.pool, self.block_table,
+                             seq_lens, seq_lens_host, self.sink, self.recent, out, workspace,
+                             self.err, softmax_scale, lse=lse, stream=stream)
+        return out
+
     def error(self) -> int:
         return binding.read_error(self.err)
 

@@ -130,13 +130,16 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   return MLA_LOWBIT_OK;
 }
 
-int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
-                      float softmax_scale, const void* q, const void* page_pool,
-                      int64_t num_pages, const int32_t* block_table, int max_pages,
-                      const int32_t* seq_lens, const int32_t* seq_lens_host,
-                      const void* sink_buf, const void* recent_buf, float* out, float* lse,
-                      void* workspace, size_t workspace_bytes, int32_t* err_word,
-                      void* stream) {
+// Decode, optionally appending one token per sequence first (ckv_new and
+// krope_new non-null): fused into the decode launch when the split kernel
+// supports it, else the writer kernel runs first on the same stream.
+static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                       float softmax_scale, const void* q, const void* ckv_new,
+                       const void* krope_new, void* page_pool, int64_t num_pages,
+                       const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                       const int32_t* seq_lens_host, void* sink_buf, void* recent_buf, float* out,
+                       float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                       void* stream) {
   int st = check_layout(layout);
   if (st != MLA_LOWBIT_OK) return st;
   if (num_seqs <= 0 || heads <= 0 || heads % 16 != 0 || heads > kMaxHeads || max_pages <= 0 ||
@@ -145,21 +148,46 @@ int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
   if ((long long)max_pages * kPageTokens > INT32_MAX) return MLA_LOWBIT_ESIZE;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MLA_LOWBIT_EINVAL;
   const bool packed = layout->content_bits != 16;
+  const bool append = ckv_new || krope_new;
   if (!q || !page_pool || !block_table || !seq_lens || !seq_lens_host || !out || !workspace ||
       !err_word)
     return MLA_LOWBIT_ENULL;
+  if (append && (!ckv_new || !krope_new)) return MLA_LOWBIT_ENULL;
   if (packed && (!sink_buf || !recent_buf)) return MLA_LOWBIT_ENULL;
   if (!aligned16(q) || !aligned16(page_pool) || !aligned16(out) || !aligned16(workspace) ||
-      (packed && (!aligned16(sink_buf) || !aligned16(recent_buf))))
+      (packed && (!aligned16(sink_buf) || !aligned16(recent_buf))) ||
+      (append && (!aligned16(ckv_new) || !aligned16(krope_new))))
     return MLA_LOWBIT_EALIGN;
-  for (int b = 0; b < num_seqs; ++b)
+  for (int b = 0; b < num_seqs; ++b) {
     if (seq_lens_host[b] < 0 || (long long)seq_lens_host[b] > (long long)max_pages * kPageTokens)
       return MLA_LOWBIT_EINVAL;
+    if (append && seq_lens_host[b] < 1) return MLA_LOWBIT_EINVAL;
+  }
   int total = 0, chunk = 0;
   size_t need = 0;
   st = mla_lowbit_decode_plan(layout, num_seqs, heads, seq_lens_host, 0, &total, &chunk, &need);
   if (st != MLA_LOWBIT_OK) return st;
   if (workspace_bytes < need) return MLA_LOWBIT_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool fused = append && decode_fuses_append(layout->content_bits);
+  if (append && !fused) {
+    WriterArgs w;
+    w.ckv = static_cast<const uint32_t*>(ckv_new);
+    w.krope = static_cast<const uint32_t*>(krope_new);
+    w.seq_idx = nullptr;
+    w.pos = nullptr;  // position seq_lens[b] - 1
+    w.lens_after = seq_lens;
+    w.block_table = block_table;
+    w.pool = static_cast<uint8_t*>(page_pool);
+    w.sink = static_cast<uint32_t*>(sink_buf);
+    w.recent = static_cast<uint32_t*>(recent_buf);
+    w.err = err_word;
+    w.num_pages = num_pages;
+    w.n_tokens = num_seqs;
+    w.num_seqs = num_seqs;
+    w.max_pages = max_pages;
+    if (launch_writer(layout->content_bits, w, s) != cudaSuccess) return MLA_LOWBIT_ECUDA;
+  }
   DecodeArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.pool = static_cast<const uint8_t*>(page_pool);
@@ -178,9 +206,41 @@ int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
   a.chunk_pages = chunk;
   a.total_splits = total;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
-  cudaError_t e =
-      launch_decode(layout->content_bits, a, out, lse, static_cast<cudaStream_t>(stream));
+  if (fused) {
+    a.new_ckv = static_cast<const uint32_t*>(ckv_new);
+    a.new_kr = static_cast<const uint32_t*>(krope_new);
+    a.pool_w = static_cast<uint8_t*>(page_pool);
+    a.sink_w = static_cast<uint32_t*>(sink_buf);
+    a.recent_w = static_cast<uint32_t*>(recent_buf);
+  }
+  cudaError_t e = launch_decode(layout->content_bits, a, out, lse, s);
   return e == cudaSuccess ? MLA_LOWBIT_OK : MLA_LOWBIT_ECUDA;
+}
+
+int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                      float softmax_scale, const void* q, const void* page_pool,
+                      int64_t num_pages, const int32_t* block_table, int max_pages,
+                      const int32_t* seq_lens, const int32_t* seq_lens_host,
+                      const void* sink_buf, const void* recent_buf, float* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int32_t* err_word,
+                      void* stream) {
+  return decode_impl(layout, num_seqs, heads, softmax_scale, q, nullptr, nullptr,
+                     const_cast<void*>(page_pool), num_pages, block_table, max_pages, seq_lens,
+                     seq_lens_host, const_cast<void*>(sink_buf), const_cast<void*>(recent_buf), out,
+                     lse, workspace, workspace_bytes, err_word, stream);
+}
+
+int mla_lowbit_write_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                            float softmax_scale, const void* q, const void* ckv_new,
+                            const void* krope_new, void* page_pool, int64_t num_pages,
+                            const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                            const int32_t* seq_lens_host, void* sink_buf, void* recent_buf,
+                            float* out, float* lse, void* workspace, size_t workspace_bytes,
+                            int32_t* err_word, void* stream) {
+  if (!ckv_new || !krope_new) return MLA_LOWBIT_ENULL;
+  return decode_impl(layout, num_seqs, heads, softmax_scale, q, ckv_new, krope_new, page_pool,
+                     num_pages, block_table, max_pages, seq_lens, seq_lens_host, sink_buf,
+                     recent_buf, out, lse, workspace, workspace_bytes, err_word, stream);
 }
 
 int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out) {

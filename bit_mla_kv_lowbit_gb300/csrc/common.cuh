@@ -137,11 +137,22 @@ struct DecodeArgs {
   int32_t* err;
   int B, H, max_pages, chunk_pages, total_splits;
   float scale_log2;  // softmax_scale * log2(e)
+  // Fused append (mla_lowbit_write_decode): the token at position
+  // seq_lens[b] - 1 of every sequence, written by the sequence's bf16 split of
+  // head chunk 0 and read from here by every bf16 split.  Null for a plain decode.
+  const uint32_t* new_ckv = nullptr;  // [B][256] bf16 pairs
+  const uint32_t* new_kr = nullptr;   // [B][32] bf16 pairs
+  uint8_t* pool_w = nullptr;          // the page pool, writable
+  uint32_t* sink_w = nullptr;         // [B][4][288] bf16 pairs
+  uint32_t* recent_w = nullptr;       // [B][128][288] bf16 pairs
 };
 
 cudaError_t launch_writer(int cbits, const WriterArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream);
+// True when launch_decode can append each sequence's new token itself (the
+// DecodeArgs new_* fields): the default split kernel on a packed layout.
+bool decode_fuses_append(int cbits);
 cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_hy(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_gw(int cbits, const DecodeArgs& a, cudaStream_t stream);

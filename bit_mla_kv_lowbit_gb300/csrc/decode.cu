@@ -29,6 +29,7 @@
 #include <cstdlib>
 
 #include "decode_common.cuh"
+#include "writer_common.cuh"
 
 namespace mlalb {
 
@@ -202,6 +203,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     __syncthreads();
   }
 
+  // fused append: the sequence's new token (position L - 1) is packed into its
+  // page and copied to the bf16 buffers by head chunk 0's bf16 split, one warp
+  // per group.  No split reads those bytes in this call: the token is inside
+  // the recent window, and every bf16 split reads it from the input below.
+  if constexpr (kPacked) {
+    if (bf16_split && a.new_ckv && hc == 0 && L >= 1 && (tid >> 5) < kGroups) {
+      const int gwp = tid >> 5, pos = L - 1;
+      const long long page = a.block_table[(long long)b * a.max_pages + pos / kPageTokens];
+      if (page >= 0 && page < a.num_pages) {
+        const uint32_t v = gwp < 8 ? a.new_ckv[(long long)b * (kLatent / 2) + gwp * 32 + lane]
+                                   : a.new_kr[(long long)b * (kRope / 2) + lane];
+        if (pos < kSink) a.sink_w[((long long)b * kSink + pos) * (kDim / 2) + gwp * 32 + lane] = v;
+        a.recent_w[((long long)b * kLocal + pos % kLocal) * (kDim / 2) + gwp * 32 + lane] = v;
+        write_packed_group<CB>(a.pool_w + page * G.page_bytes, pos % kPageTokens, gwp, lane, v);
+      } else if (tid == 0) {
+        set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+      }
+    }
+  }
+
   float O[8][4];
 #pragma unroll
   for (int c = 0; c < 8; ++c) O[c][0] = O[c][1] = O[c][2] = O[c][3] = 0.f;
@@ -304,12 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     } else {
       // bf16 rows: protected tokens of a packed cache, or bf16 pages.
       const uint16_t* rowptr = nullptr;
+      const uint16_t* rope_ptr = nullptr;  // RoPE channels, when not at rowptr + 512
       if (bf16_split) {
         const int i = tile_i * kPageTokens + rowB;
         if (i < n_tok) {
           const int pos = i < n_sink ? i : rec_start + (i - n_sink);
-          rowptr = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
-                               : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
+          if (a.new_ckv && pos == L - 1) {
+            rowptr = reinterpret_cast<const uint16_t*>(a.new_ckv) + (long long)b * kLatent;
+            rope_ptr = reinterpret_cast<const uint16_t*>(a.new_kr) + (long long)b * kRope;
+          } else {
+            rowptr = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
+                                 : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
+          }
         }
         v0 = tile_i * kPageTokens + tC0 < n_tok;
         v1 = tile_i * kPageTokens + tC0 + 1 < n_tok;
@@ -328,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       for (int g = 0; g < kGroups; ++g) {
         uint32_t vv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (rowptr) {
-          const uint4* src = reinterpret_cast<const uint4*>(rowptr + g * 64 + j * 16);
+          const uint16_t* chan = (g == 8 && rope_ptr) ? rope_ptr : rowptr + g * 64;
+          const uint4* src = reinterpret_cast<const uint4*>(chan + j * 16);
           const uint4 t0 = src[0], t1 = src[1];
           vv[0] = t0.x; vv[1] = t0.y; vv[2] = t0.z; vv[3] = t0.w;
           vv[4] = t1.x; vv[5] = t1.y; vv[6] = t1.z; vv[7] = t1.w;
@@ -637,6 +665,10 @@ static SplitKernel split_kernel(int cbits) {
   if (v && v[0] == 't') return SplitKernel::kTc;
   if (v && v[0] == 'g') return SplitKernel::kGroupWarp;
   return SplitKernel::kMma;
+}
+
+bool decode_fuses_append(int cbits) {
+  return cbits != 16 && split_kernel(cbits) == SplitKernel::kMma;
 }
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,

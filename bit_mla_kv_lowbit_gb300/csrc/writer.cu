@@ -8,7 +8,7 @@
 // bf16 copies.  The arithmetic is the float32 definition in mla_lowbit.h, done
 // with explicitly rounded intrinsics so that it is bit-exact regardless of
 // compiler contraction.
-#include "common.cuh"
+#include "writer_common.cuh"
 
 namespace mlalb {
 
@@ -20,7 +20,11 @@ __global__ void __launch_bounds__(kGroups * 32) writer_kernel(WriterArgs a) {
   const int lane = threadIdx.x & 31;
 
   const int s = a.seq_idx ? a.seq_idx[i] : i;
-  const int p = a.pos[i];
+  if (!a.pos && (s < 0 || s >= a.num_seqs)) {  // appending: token i is sequence i's
+    if (threadIdx.x == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_SEQ);
+    return;
+  }
+  const int p = a.pos ? a.pos[i] : a.lens_after[s] - 1;
   if (s < 0 || s >= a.num_seqs) {
     if (threadIdx.x == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_SEQ);
     return;
@@ -51,44 +55,7 @@ __global__ void __launch_bounds__(kGroups * 32) writer_kernel(WriterArgs a) {
     if (p >= len_after - kLocal)
       a.recent[((long long)s * kLocal + p % kLocal) * (kDim / 2) + g * 32 + lane] = v;
 
-    const int bits = g < 8 ? CB : 4;
-    const int levels = (1 << bits) - 1;
-    const float x0 = bf16lo_to_f32(v), x1 = bf16hi_to_f32(v);
-    float mn = fminf(x0, x1), mx = fmaxf(x0, x1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    mn = __fadd_rn(mn, 0.0f);  // a zero minimum is stored as +0
-    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
-    const __half s16 = __float2half_rn(fminf(s32, 65504.0f));
-    const __half m16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
-    const float sf = __half2float(s16), mf = __half2float(m16);
-    int c0 = 0, c1 = 0;
-    if (sf != 0.0f) {
-      c0 = __float2int_rn(__fdiv_rn(__fsub_rn(x0, mf), sf));
-      c1 = __float2int_rn(__fdiv_rn(__fsub_rn(x1, mf), sf));
-      c0 = min(max(c0, 0), levels);
-      c1 = min(max(c1, 0), levels);
-    }
-    uint8_t* seg;
-    if (g < 8)
-      seg = base + G.content_off + row * G.content_row + g * (G.content_row / 8);
-    else
-      seg = base + G.rope_off + row * G.rope_row;
-    if (bits == 4) {
-      seg[lane] = static_cast<uint8_t>(c0 | (c1 << 4));
-    } else {
-      const int nib = c0 | (c1 << 2);
-      const int other = __shfl_down_sync(0xffffffffu, nib, 1);
-      if ((lane & 1) == 0) seg[lane >> 1] = static_cast<uint8_t>(nib | (other << 4));
-    }
-    if (lane == 0) {
-      const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
-                            (static_cast<uint32_t>(__half_as_ushort(m16)) << 16);
-      *reinterpret_cast<uint32_t*>(base + G.meta_off + row * G.meta_row + g * 4) = meta;
-    }
+    write_packed_group<CB>(base, row, g, lane, v);
   }
 }
 

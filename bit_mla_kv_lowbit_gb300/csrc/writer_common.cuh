@@ -1,0 +1,61 @@
+// The writer's arithmetic for one 64-channel group of one token, shared by the
+// stand-alone writer kernel and the decode kernel's fused append.
+//
+// QuantMLA, Figure 8 caption: every incoming token is packed as it arrives.
+// One warp quantises one group: lane l holds channels (2l, 2l+1) as a bf16
+// pair; a warp-wide min/max gives the fp16 scale and min (float32 arithmetic
+// with explicitly rounded intrinsics, so the bytes are independent of
+// compiler contraction), codes are rounded half to even, clamped and packed.
+#pragma once
+
+#include "common.cuh"
+
+namespace mlalb {
+
+// Quantise and store group g (0..7 content, 8 RoPE) of the token in row `row`
+// of the packed page at `page_base`.  All 32 lanes of the warp must call it.
+template <int CB>
+__device__ __forceinline__ void write_packed_group(uint8_t* page_base, int row, int g, int lane,
+                                                   uint32_t v) {
+  constexpr PageGeom G = page_geom(CB);
+  const int bits = g < 8 ? CB : 4;
+  const int levels = (1 << bits) - 1;
+  const float x0 = bf16lo_to_f32(v), x1 = bf16hi_to_f32(v);
+  float mn = fminf(x0, x1), mx = fmaxf(x0, x1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  mn = __fadd_rn(mn, 0.0f);  // a zero minimum is stored as +0
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+  const __half s16 = __float2half_rn(fminf(s32, 65504.0f));
+  const __half m16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
+  const float sf = __half2float(s16), mf = __half2float(m16);
+  int c0 = 0, c1 = 0;
+  if (sf != 0.0f) {
+    c0 = __float2int_rn(__fdiv_rn(__fsub_rn(x0, mf), sf));
+    c1 = __float2int_rn(__fdiv_rn(__fsub_rn(x1, mf), sf));
+    c0 = min(max(c0, 0), levels);
+    c1 = min(max(c1, 0), levels);
+  }
+  uint8_t* seg;
+  if (g < 8)
+    seg = page_base + G.content_off + row * G.content_row + g * (G.content_row / 8);
+  else
+    seg = page_base + G.rope_off + row * G.rope_row;
+  if (bits == 4) {
+    seg[lane] = static_cast<uint8_t>(c0 | (c1 << 4));
+  } else {
+    const int nib = c0 | (c1 << 2);
+    const int other = __shfl_down_sync(0xffffffffu, nib, 1);
+    if ((lane & 1) == 0) seg[lane >> 1] = static_cast<uint8_t>(nib | (other << 4));
+  }
+  if (lane == 0) {
+    const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
+                          (static_cast<uint32_t>(__half_as_ushort(m16)) << 16);
+    *reinterpret_cast<uint32_t*>(page_base + G.meta_off + row * G.meta_row + g * 4) = meta;
+  }
+}
+
+}  // namespace mlalb

@@ -174,6 +174,31 @@ int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
                       void* workspace, size_t workspace_bytes, int32_t* err_word,
                       void* stream);
 
+/* One decode step with its append (QuantMLA, Figure 8 caption: the writer packs
+ * every incoming token and attention runs over the packed cache and the bf16
+ * buffers): writes the token at position seq_lens[s] - 1 of every sequence
+ * exactly as mla_lowbit_write does with pos = seq_lens[s] - 1 and
+ * seq_lens_after = seq_lens, then decodes exactly as mla_lowbit_decode over
+ * seq_lens[s] tokens.  Results (pool bytes, bf16 buffers, out, lse) are
+ * identical to that pair of calls.  For packed layouts on the default split
+ * kernel both happen in the decode launch (the new token is inside the recent
+ * window, so no packed split reads the bytes being written, and the bf16
+ * split reads the new values from ckv_new/krope_new); otherwise the writer
+ * kernel runs first on `stream`.
+ *
+ *   ckv_new    [num_seqs][512] bf16, krope_new [num_seqs][64] bf16 (16-byte aligned)
+ *   seq_lens   device, every entry >= 1 (seq_lens_host the same values)
+ *   page_pool, sink_buf, recent_buf are written (as by mla_lowbit_write)
+ * Other arguments, errors and the workspace as for mla_lowbit_decode;
+ * seq_lens_host entries < 1 return MLA_LOWBIT_EINVAL. */
+int mla_lowbit_write_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
+                            float softmax_scale, const void* q, const void* ckv_new,
+                            const void* krope_new, void* page_pool, int64_t num_pages,
+                            const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                            const int32_t* seq_lens_host, void* sink_buf, void* recent_buf,
+                            float* out, float* lse, void* workspace, size_t workspace_bytes,
+                            int32_t* err_word, void* stream);
+
 /* mla_lowbit_decode for callers that cannot allocate device memory.  The
  * pages have no counterpart to this entry point: it exists because some hosts
  * give a kernel only its inputs and outputs -- a serving engine that has

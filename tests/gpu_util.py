@@ -80,17 +80,26 @@ class GpuRun:
         q = np.stack([syn.queries(self.w, b)[s] for b in range(B)])
         return ckv, kr, q
 
-    def run_step(self, s, lse=False):
-        """Writer for step s then decode over lens + s.  Returns (out, lse)."""
+    def run_step(self, s, lse=False, fused=False):
+        """Writer for step s then decode over lens + s (one mla_lowbit_write_decode
+        call when ``fused``).  Returns (out, lse)."""
         torch = self.torch
         ckv, kr, q = self.step_inputs(s)
         pos = (self.lens - 1 + s).astype(np.int32)
         lens_now = (self.lens + s).astype(np.int32)
+        lse_t = (torch.empty(self.w.batch, self.w.heads, dtype=torch.float32, device=self.dev)
+                 if lse else None)
+        if fused:
+            out = self.cache.write_decode(
+                to_dev(ckv, torch.bfloat16, self.dev), to_dev(kr, torch.bfloat16, self.dev),
+                to_dev(q, torch.bfloat16, self.dev), to_dev(lens_now, torch.int32, self.dev),
+                lens_now, self.w.softmax_scale, lse=lse_t)
+            torch.cuda.synchronize()
+            self.step = s
+            return out.cpu().numpy(), (lse_t.cpu().numpy() if lse else None)
         self.cache.write(to_dev(ckv, torch.bfloat16, self.dev), to_dev(kr, torch.bfloat16, self.dev),
                          to_dev(pos, torch.int32, self.dev),
                          seq_lens_after=to_dev(lens_now, torch.int32, self.dev))
-        lse_t = (torch.empty(self.w.batch, self.w.heads, dtype=torch.float32, device=self.dev)
-                 if lse else None)
         out = self.cache.decode(to_dev(q, torch.bfloat16, self.dev),
                                 to_dev(lens_now, torch.int32, self.dev), lens_now,
                                 self.w.softmax_scale, lse=lse_t)

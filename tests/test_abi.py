@@ -116,6 +116,24 @@ def test_decode_host_validation_without_launch():
     assert _call_decode(lay, lens_host=too_long.ctypes.data) == -1
 
 
+def _call_write_decode(lay, B=2, H=16, ckv=0x8000, kr=0x9000, lens_host=None):
+    # fake, aligned device pointers: every case is rejected before any launch
+    lens = np.array([100, 300], np.int32) if lens_host is None else lens_host
+    return pkg.load().mla_lowbit_write_decode(
+        ctypes.byref(lay), B, H, ctypes.c_float(0.07), 0x1000, ckv, kr, 0x2000, 64, 0x3000, 16,
+        0x4000, lens.ctypes.data, 0x5000, 0x6000, 0x7000, None, 0xA000, 1 << 20, 0xB000, None)
+
+
+def test_write_decode_host_validation_without_launch():
+    lay = pkg.layout(4, 4)
+    assert _call_write_decode(lay, ckv=None) == -2
+    assert _call_write_decode(lay, kr=None) == -2
+    assert _call_write_decode(lay, ckv=0x8008) == -3          # new-token rows not 16-byte aligned
+    zero = np.array([100, 0], np.int32)                        # every sequence appends a token
+    assert _call_write_decode(lay, lens_host=zero) == -1
+    assert _call_write_decode(lay, H=24) == -4
+
+
 def _expected_splits(L, packed, chunk):
     # Packed layouts: pages that hold at least one token served from packed codes
     # (positions 4 .. L-129), cut into chunks, plus one split for the bf16 tokens.

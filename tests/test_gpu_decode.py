@@ -19,8 +19,8 @@ EDGE_LENGTHS = [1, 2, 4, 5, 63, 64, 65, 100, 131, 132, 133, 134, 192, 196, 197, 
                 1500, 4099]
 
 
-def _check_run_step(run, s, seqs=None, lse=None):
-    out, lse_got = run.run_step(s, lse=lse is not None)
+def _check_run_step(run, s, seqs=None, lse=None, fused=False):
+    out, lse_got = run.run_step(s, lse=lse is not None, fused=fused)
     assert run.cache.error() == 0, f"device error word {run.cache.error()}"
     seqs = range(run.w.batch) if seqs is None else seqs
     for b in seqs:
