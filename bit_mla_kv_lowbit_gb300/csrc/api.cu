@@ -106,15 +106,13 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   long long work = 0;
   for (int b = 0; b < num_seqs; ++b) {
     if (seq_lens_host[b] < 0) return MLA_LOWBIT_EINVAL;
-    work += packed_pages_of(seq_lens_host[b], packed);
+    work += units_of(seq_lens_host[b], packed);
   }
   const long long head_chunks = heads / 16;
   const long long slots = (long long)num_sms * kCtasPerSm;
-  // packed layouts add one bf16 split per sequence: leave room for them in the
-  // same wave when there are few sequences
-  long long avail = slots - (packed ? (long long)num_seqs * head_chunks : 0);
-  if (avail < slots / 2) avail = slots / 2;
-  long long chunk = (work * head_chunks + avail - 1) / avail;
+  // equal chunks of work units (pages, then the protected tokens' bf16 tiles)
+  // so that all splits of all head chunks fit one wave when they can
+  long long chunk = (work * head_chunks + slots - 1) / slots;
   if (chunk < 1) chunk = 1;
   // a split accumulates at most kMaxChunkPages * 64 tokens in fp32 tensor-core
   // accumulators (whose adds are not round-to-nearest); longer sequences get

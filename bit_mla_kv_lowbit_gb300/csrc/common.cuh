@@ -90,8 +90,10 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* p) {
                : "r"(a));
 }
 
-// Split planning shared by host and device: pages of a sequence that hold at
-// least one packed-served token, and the number of splits.
+// Split planning shared by host and device.
+//
+// Pages of a sequence that hold at least one packed-served token (for bf16
+// pages: every page).
 __host__ __device__ inline int packed_pages_of(int L, bool packed) {
   if (L <= 0) return 0;
   if (!packed) return (L + kPageTokens - 1) / kPageTokens;
@@ -99,11 +101,28 @@ __host__ __device__ inline int packed_pages_of(int L, bool packed) {
   // packed-served tokens are 4 .. L-129
   return (L - kLocal - 1) / kPageTokens + 1;
 }
-
+// Protected tokens a packed layout serves from its bf16 buffers: the sink
+// tokens 0 .. min(L,4)-1, then the recent tokens max(4, L-128) .. L-1.
+__host__ __device__ inline int bf16_tokens_of(int L, bool packed) {
+  if (!packed || L <= 0) return 0;
+  const int n_sink = L < kSink ? L : kSink;
+  const int rec_start = L - kLocal > kSink ? L - kLocal : kSink;
+  return n_sink + (L > rec_start ? L - rec_start : 0);
+}
+// Work units of a sequence: its pages (above), one unit each, then its
+// protected bf16 tokens in 64-token tiles of kBf16TileUnits units each (a tile
+// of bf16 rows read from the bf16 buffers costs about that many packed pages).
+// Splits cut the units into chunks of chunk_pages; a bf16 tile belongs to the
+// split that holds its first unit.
+constexpr int kBf16TileUnits = 3;
+__host__ __device__ inline int bf16_tiles_of(int L, bool packed) {
+  return (bf16_tokens_of(L, packed) + kPageTokens - 1) / kPageTokens;
+}
+__host__ __device__ inline int units_of(int L, bool packed) {
+  return packed_pages_of(L, packed) + kBf16TileUnits * bf16_tiles_of(L, packed);
+}
 __host__ __device__ inline int splits_of(int L, bool packed, int chunk_pages) {
-  int pages = packed_pages_of(L, packed);
-  int s = (pages + chunk_pages - 1) / chunk_pages;
-  if (packed) return s + 1;  // + the bf16 (sink/recent) split
+  const int s = (units_of(L, packed) + chunk_pages - 1) / chunk_pages;
   return s > 0 ? s : 1;
 }
 

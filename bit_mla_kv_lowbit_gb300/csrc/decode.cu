@@ -123,27 +123,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     a.seq_split[2 * b + 1] = nsplit;
   }
 
-  // ---- work of this split
-  const bool bf16_split = kPacked && split == nsplit - 1;
-  int n_tiles, page_begin = 0, n_sink = 0, rec_start = 0, n_tok = 0;
-  if (bf16_split) {
-    n_sink = min(L, kSink);
-    rec_start = max(kSink, L - kLocal);
-    n_tok = n_sink + max(0, L - rec_start);
-    n_tiles = (n_tok + kPageTokens - 1) / kPageTokens;
-  } else {
-    const int pages = packed_pages_of(L, kPacked);
-    page_begin = split * a.chunk_pages;
-    n_tiles = max(0, min(a.chunk_pages, pages - page_begin));
-  }
-  if (n_tiles > 64) {  // the planner caps splits at 64 pages
+  // ---- work of this split: pages, then 64-token tiles of the protected bf16
+  // tokens (packed layouts); tile_i < n_pages is a page
+  const SplitWork sw = split_work(L, split, a.chunk_pages, kPacked);
+  const int n_pages = sw.n_pages, page_begin = sw.page_begin;
+  int n_tiles = n_pages + sw.n_bf;
+  if (n_tiles > 64) {  // the planner caps splits at 64 units
     if (tid == 0) set_error(a.err, MLA_LOWBIT_DEV_PLAN);
     n_tiles = 0;
   }
   const int valid_lo = kPacked ? kSink : 0;
   const int valid_hi = kPacked ? L - kLocal : L;  // packed-served tokens [lo, hi)
-  bool use_stage = false;
-  if constexpr (kPacked) use_stage = !bf16_split;
 
   // Copy packed page `tile_i` of this split into the team's staging buffer.
   auto stage_page = [&](int tile_i) {
@@ -196,10 +186,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       }
       qsum[g * kHC + h] = acc;
     }
-    if (kPacked && !bf16_split && tid < n_tiles && tid < 64)
+    if (kPacked && tid < n_pages && tid < 64)
       s_pages[tid] = a.block_table[(long long)b * a.max_pages + page_begin + tid];
+    if constexpr (kPacked) {
+      // the bf16 rows of this split's protected-token tiles come last and are
+      // read straight from the bf16 buffers: start moving them into L2 now
+      const int first = 64 * sw.bf_begin, end = min(sw.n_tok, 64 * (sw.bf_begin + sw.n_bf));
+      for (int k = tid; k < (end - first) * (kDim * 2 / 128); k += kThreads) {
+        const int pos = bf16_pos(sw, first + k / (kDim * 2 / 128));
+        const uint16_t* row = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
+                                          : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + (k % (kDim * 2 / 128)) * 64));
+      }
+    }
     __syncthreads();  // page ids visible
-    if (use_stage && team < n_tiles) stage_page(team);
+    if (kPacked && team < n_pages) stage_page(team);
     __syncthreads();
   }
 
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   // per group.  No split reads those bytes in this call: the token is inside
   // the recent window, and every bf16 split reads it from the input below.
   if constexpr (kPacked) {
-    if (bf16_split && a.new_ckv && hc == 0 && L >= 1 && (tid >> 5) < kGroups) {
+    if (sw.has_last && a.new_ckv && hc == 0 && L >= 1 && (tid >> 5) < kGroups) {
       const int gwp = tid >> 5, pos = L - 1;
       const long long page = a.block_table[(long long)b * a.max_pages + pos / kPageTokens];
       if (page >= 0 && page < a.num_pages) {
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   const int tC0 = warp * 8 + 2 * j;  // tile rows of this thread's C columns
 
   for (int tile_i = team; tile_i < n_tiles; tile_i += kTeams) {
+    const bool use_stage = kPacked && tile_i < n_pages;  // a staged packed page
     if (use_stage) cp_async_wait_all();
     team_sync(team);
     // ================= phase 1: unpack + QK for tokens 8w..8w+7
@@ -326,10 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       // bf16 rows: protected tokens of a packed cache, or bf16 pages.
       const uint16_t* rowptr = nullptr;
       const uint16_t* rope_ptr = nullptr;  // RoPE channels, when not at rowptr + 512
-      if (bf16_split) {
-        const int i = tile_i * kPageTokens + rowB;
-        if (i < n_tok) {
-          const int pos = i < n_sink ? i : rec_start + (i - n_sink);
+      if (kPacked) {
+        // protected tokens: tile (bf_begin + tile_i - n_pages) of the bf16 list
+        const int bt = sw.bf_begin + tile_i - n_pages;
+        const int i = bt * kPageTokens + rowB;
+        if (i < sw.n_tok) {
+          const int pos = bf16_pos(sw, i);
           if (a.new_ckv && pos == L - 1) {
             rowptr = reinterpret_cast<const uint16_t*>(a.new_ckv) + (long long)b * kLatent;
             rope_ptr = reinterpret_cast<const uint16_t*>(a.new_kr) + (long long)b * kRope;
@@ -338,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
                                  : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
           }
         }
-        v0 = tile_i * kPageTokens + tC0 < n_tok;
-        v1 = tile_i * kPageTokens + tC0 + 1 < n_tok;
+        v0 = bt * kPageTokens + tC0 < sw.n_tok;
+        v1 = bt * kPageTokens + tC0 + 1 < sw.n_tok;
       } else {
         const int page_idx = page_begin + tile_i;
         const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
     }
     team_sync(team);
     // the staging buffer is free again: fetch this team's next page
-    if (use_stage && tile_i + kTeams < n_tiles) stage_page(tile_i + kTeams);
+    if (kPacked && tile_i + kTeams < n_pages) stage_page(tile_i + kTeams);
     float t0 = -INFINITY, t1 = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kTeamWarps; ++w) {

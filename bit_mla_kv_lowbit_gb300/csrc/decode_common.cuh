@@ -101,6 +101,41 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
   lo = pack_half2(a - hf.x, b - hf.y);
 }
 
+// ---------------------------------------------------------------- split work
+// Units [split * chunk, (split + 1) * chunk) of a sequence of length L: packed
+// pages page_begin .. page_begin + n_pages - 1, then bf16 tiles bf_begin ..
+// bf_begin + n_bf - 1 (the tiles whose first unit falls in the range); bf16
+// tile k holds protected tokens 64k .. 64k + 63 of the list (sink tokens
+// 0 .. n_sink - 1, then recent tokens from rec_start), n_tok in all, in
+// bf_total tiles.  has_last: the split holds the last protected token.
+struct SplitWork {
+  int page_begin, n_pages, bf_begin, n_bf, n_sink, rec_start, n_tok, bf_total;
+  bool has_last;
+};
+__device__ __forceinline__ SplitWork split_work(int L, int split, int chunk, bool packed) {
+  SplitWork w;
+  const int pages = packed_pages_of(L, packed);
+  const int u0 = split * chunk, u1 = min(units_of(L, packed), u0 + chunk);
+  w.page_begin = u0;
+  w.n_pages = max(0, min(u1, pages) - u0);
+  w.bf_total = bf16_tiles_of(L, packed);
+  // first unit of tile k is pages + kBf16TileUnits * k
+  const int k0 = max(0, (u0 - pages + kBf16TileUnits - 1) / kBf16TileUnits);
+  const int k1 = min(w.bf_total, max(0, (u1 - pages + kBf16TileUnits - 1) / kBf16TileUnits));
+  w.bf_begin = min(k0, w.bf_total);
+  w.n_bf = max(0, k1 - w.bf_begin);
+  w.n_sink = packed ? min(L, kSink) : 0;
+  w.rec_start = max(kSink, L - kLocal);
+  w.n_tok = bf16_tokens_of(L, packed);
+  w.has_last = w.n_bf > 0 && w.bf_begin + w.n_bf == w.bf_total;
+  return w;
+}
+
+// Position of entry idx of the protected-token list.
+__device__ __forceinline__ int bf16_pos(const SplitWork& w, int idx) {
+  return idx < w.n_sink ? idx : w.rec_start + (idx - w.n_sink);
+}
+
 // ---------------------------------------------------------------- plan lookup
 // Every CTA recomputes the per-sequence split counts (same integer formula as
 // the host) and finds which (sequence, split) its blockIdx.x names.

@@ -100,19 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
     a.seq_split[2 * b + 1] = nsplit;
   }
 
-  // ---- work of this split
-  const bool bf16_split = split == nsplit - 1;
-  int n_tiles, page_begin = 0, n_sink = 0, rec_start = 0, n_tok = 0;
-  if (bf16_split) {
-    n_sink = min(L, kSink);
-    rec_start = max(kSink, L - kLocal);
-    n_tok = n_sink + max(0, L - rec_start);
-    n_tiles = (n_tok + kPageTokens - 1) / kPageTokens;
-  } else {
-    const int pages = packed_pages_of(L, true);
-    page_begin = split * a.chunk_pages;
-    n_tiles = max(0, min(a.chunk_pages, pages - page_begin));
-  }
+  // ---- work of this split: packed pages, then 64-token tiles of the
+  // protected bf16 tokens; tile i < n_pages is a page
+  const SplitWork sw = split_work(L, split, a.chunk_pages, true);
+  const int n_pages = sw.n_pages, page_begin = sw.page_begin;
+  int n_tiles = n_pages + sw.n_bf;
   if (n_tiles > 64) {  // the planner caps splits at 64 pages
     if (tid == 0) set_error(a.err, MLA_LOWBIT_DEV_PLAN);
     n_tiles = 0;
@@ -120,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
   const int valid_lo = kSink, valid_hi = L - kLocal;  // packed-served tokens [lo, hi)
 
   auto stage_page = [&](int tile_i) {
-    if (!bf16_split && tile_i < n_tiles) {
+    if (tile_i < n_pages) {
       const long long page = s_pages[tile_i];
       if (page >= 0 && page < a.num_pages) {
         const uint8_t* src = a.pool + page * G.page_bytes;
@@ -166,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
     }
     qsum_s[g * kHC + h] = acc;
   }
-  if (!bf16_split && tid < n_tiles)
+  if (tid < n_pages && tid < 64)
     s_pages[tid] = a.block_table[(long long)b * a.max_pages + page_begin + tid];
   __syncthreads();
   stage_page(0);
@@ -193,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
   float m_run = -INFINITY, l_run = 0.f;
 
   for (int i = 0; i < n_tiles; ++i) {
-    if (!bf16_split) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();  // B0: page i staged; buffers of page i - 1 free
     stage_page(i + 2);
 
@@ -202,7 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
     float sv[4][2], mv[4][2];  // s and m' of this thread's C-fragment tokens, group g
     const int tok0 = (page_begin + i) * kPageTokens;
     bool page_ok = true;
-    if (!bf16_split) {
+    const bool bf_tile = i >= n_pages;
+    const int bt = sw.bf_begin + i - n_pages;  // bf16 tile index when bf_tile
+    if (!bf_tile) {
       const long long page = s_pages[i];
       page_ok = page >= 0 && page < a.num_pages;
       if (!page_ok && tid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
@@ -282,14 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
         const int nb = 4 * hf + nl;
         const int r = 8 * nb + rn;
         const int t0 = 8 * nb + 2 * j;
-        const int idx = i * kPageTokens + r;
+        const int idx = bt * kPageTokens + r;
         const uint16_t* rowp = nullptr;
-        if (idx < n_tok) {
-          const int pos = idx < n_sink ? idx : rec_start + (idx - n_sink);
+        if (idx < sw.n_tok) {
+          const int pos = bf16_pos(sw, idx);
           rowp = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
                              : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
         }
-        const bool v0 = i * kPageTokens + t0 < n_tok, v1 = i * kPageTokens + t0 + 1 < n_tok;
+        const bool v0 = bt * kPageTokens + t0 < sw.n_tok, v1 = bt * kPageTokens + t0 + 1 < sw.n_tok;
         uint32_t vv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (rowp) {
           const uint4* src = reinterpret_cast<const uint4*>(rowp + g * 64 + j * 16);
@@ -339,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = 2 * lane + e;
-        const bool valid = bf16_split ? (i * kPageTokens + t < n_tok)
+        const bool valid = bf_tile ? (bt * kPageTokens + t < sw.n_tok)
                                       : (page_ok && tok0 + t >= valid_lo && tok0 + t < valid_hi);
         z[e] = valid ? z[e] * a.scale_log2 : -INFINITY;
         tmax = fmaxf(tmax, z[e]);
@@ -398,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gw_kernel(DecodeArgs a) {
       }
     }
   }
-  if (!bf16_split) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 
   // ---- epilogue: min term into every channel of the group; the two halves of
   // each group are added (half 1 hands its sums over through shared memory),

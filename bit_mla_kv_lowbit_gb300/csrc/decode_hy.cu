@@ -131,19 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
     a.seq_split[2 * b + 1] = nsplit;
   }
 
-  // ---- work of this split: packed pages, or the bf16 (sink + recent) tokens
-  const bool bf16_split = split == nsplit - 1;
-  int n_tiles, page_begin = 0, n_sink = 0, rec_start = 0, n_tok = 0;
-  if (bf16_split) {
-    n_sink = min(L, kSink);
-    rec_start = max(kSink, L - kLocal);
-    n_tok = n_sink + max(0, L - rec_start);
-    n_tiles = (n_tok + kPageTokens - 1) / kPageTokens;
-  } else {
-    const int pages = packed_pages_of(L, true);
-    page_begin = split * a.chunk_pages;
-    n_tiles = max(0, min(a.chunk_pages, pages - page_begin));
-  }
+  // ---- work of this split: packed pages, then 64-token tiles of the
+  // protected bf16 tokens; tile i < n_pages is a page
+  const SplitWork sw = split_work(L, split, a.chunk_pages, true);
+  const int n_pages = sw.n_pages, page_begin = sw.page_begin;
+  int n_tiles = n_pages + sw.n_bf;
   const int valid_lo = kSink, valid_hi = L - kLocal;  // packed-served tokens [lo, hi)
   if (n_tiles > 64) {  // the planner caps splits at 64 pages
     if (tid == 0) set_error(a.err, MLA_LOWBIT_DEV_PLAN);
@@ -152,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
 
   const int ct = tid;  // compute-thread index (valid for warp < 8)
   auto stage_page = [&](int tile_i) {
-    if (!bf16_split && tile_i < n_tiles) {
+    if (tile_i < n_pages) {
       const long long page = s_pages[tile_i];
       if (page >= 0 && page < a.num_pages) {
         const uint8_t* src = a.pool + page * G.page_bytes;
@@ -214,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
     }
     qsum_s[g * kHC + h] = acc;
   }
-  if (!bf16_split && tid < n_tiles)
+  if (tid < n_pages && tid < 64)
     s_pages[tid] = a.block_table[(long long)b * a.max_pages + page_begin + tid];
   __syncthreads();  // page ids visible
-  if (warp < kComputeWarps && !bf16_split) {
+  if (warp < kComputeWarps) {
     stage_page(0);
     stage_page(1);
   }
@@ -249,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i & 1;
       uint8_t* planes = planes0 + buf * kPlaneSet;
-      if (!bf16_split) cp_async_wait<1>();
+      cp_async_wait<1>();
       // plane set `buf` is free once PV of page i - 2 has finished
       if (i >= 2 && !local_abort &&
           !bar_wait(bar(kBarPVDone + buf), ((i - 2) >> 1) & 1, abort_flag, a.err))
@@ -260,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
       float S[4] = {0.f, 0.f, 0.f, 0.f};
       float mp0[8], mp1[8];  // m' of tokens tC0, tC0 + 1 (0 when invalid)
       bool v0, v1, big = false;
-      if (!bf16_split) {
+      if (i < n_pages) {
         const int page_idx = page_begin + i;
         const long long page = s_pages[i];
         const bool page_ok = page >= 0 && page < a.num_pages;
@@ -336,14 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
       } else {
         // bf16 rows of the protected tokens: values in place of codes, s = 1, m = 0
         const uint16_t* rowptr = nullptr;
-        const int idx = i * kPageTokens + rowB;
-        if (idx < n_tok) {
-          const int pos = idx < n_sink ? idx : rec_start + (idx - n_sink);
+        const int bt = sw.bf_begin + i - n_pages;
+        const int idx = bt * kPageTokens + rowB;
+        if (idx < sw.n_tok) {
+          const int pos = bf16_pos(sw, idx);
           rowptr = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
                                : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
         }
-        v0 = i * kPageTokens + tC0 < n_tok;
-        v1 = i * kPageTokens + tC0 + 1 < n_tok;
+        v0 = bt * kPageTokens + tC0 < sw.n_tok;
+        v1 = bt * kPageTokens + tC0 + 1 < sw.n_tok;
 #pragma unroll 1
         for (int g = 0; g < kGroups; ++g) {
           uint32_t vv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -406,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
       if (lane == 0) flags[warp] = (vote_need ? 1 : 0) | (vote_abort ? 2 : 0);
       bar_sync_compute();  // B1
       // the staged page has been read by every compute thread: fetch page i + 2
-      if (!bf16_split) stage_page(i + 2);
+      stage_page(i + 2);
       int fl = 0;
 #pragma unroll
       for (int w = 0; w < kComputeWarps; ++w) fl |= flags[w];
@@ -522,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_hy_kernel(DecodeArgs a) {
       bar_arrive(bar(kBarPReady));
       done_tiles = i + 1;
     }
-    if (!bf16_split) cp_async_wait<0>();
+    cp_async_wait<0>();
 
     // -------- epilogue: wait for the last PV, reduce the register terms,
     // write the partial

@@ -120,19 +120,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     a.seq_split[2 * b + 1] = nsplit;
   }
 
-  // ---- work of this split: packed pages (two tiles each) or the bf16 tokens
-  const bool bf16_split = split == nsplit - 1;
-  int n_tiles, page_begin = 0, n_sink = 0, rec_start = 0, n_tok = 0;
-  if (bf16_split) {
-    n_sink = min(L, kSink);
-    rec_start = max(kSink, L - kLocal);
-    n_tok = n_sink + max(0, L - rec_start);
-    n_tiles = (n_tok + kTok - 1) / kTok;
-  } else {
-    const int pages = packed_pages_of(L, true);
-    page_begin = split * a.chunk_pages;
-    n_tiles = 2 * max(0, min(a.chunk_pages, pages - page_begin));
-  }
+  // ---- work of this split: packed pages (two tiles each), then the
+  // protected bf16 tokens of its bf16 units in 32-token tiles
+  const SplitWork sw = split_work(L, split, a.chunk_pages, true);
+  const int page_begin = sw.page_begin, n_pk = 2 * sw.n_pages;
+  const int bf_first = 64 * sw.bf_begin;  // first protected-token index of the split
+  const int bf_end = min(sw.n_tok, 64 * (sw.bf_begin + sw.n_bf));
+  const int n_tiles = n_pk + max(0, (bf_end - bf_first + kTok - 1) / kTok);
 
   // ---- set-up: barriers, TMEM, q planes, zero regions
   if (tid == 0) {
@@ -206,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
     auto stage_at = [&](int s, int unit) { return sStage + s * kStageBytes + unit * 2048 + u * 16; };
     auto issue = [&](int i) {
       uint8_t okb = 0;
-      if (i < n_tiles && !bf16_split) {
+      if (i < n_pk) {
         const int page_idx = page_begin + (i >> 1);
         const int r = (i & 1) * kTok + t;
         const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
@@ -237,10 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       if (i < n_tiles) sValid[(i % kStages) * 128 + u] = okb;
       cp_async_commit();
     };
-    if (!bf16_split) {
-      issue(0);
-      issue(1);
-    }
+    issue(0);
+    issue(1);
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i % kNB;
       if (i >= kNB && !bar_wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err))
@@ -249,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
       uint32_t* meta = sMeta + buf * 9 * kTok;
       uint8_t* mm = A + 9 * kPlane;
       const float centre = kTypeB ? float(kCentre2) : float(kCentre4);
-      if (!bf16_split) {
-        issue(i + 2);
+      issue(i + 2);
+      if (i < n_pk) {
         cp_async_wait<2>();
         const int s = i % kStages;
         const uint8_t okb = sValid[s * 128 + u];
@@ -319,11 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         }
       } else {
         // bf16 rows (protected tokens): values in place of codes, scale 1, min 0
-        const int idx = i * kTok + t;
-        const bool okt = idx < n_tok;
+        const int idx = bf_first + (i - n_pk) * kTok + t;
+        const bool okt = idx < bf_end;
         const uint16_t* rp = nullptr;
         if (okt) {
-          const int pos = idx < n_sink ? idx : rec_start + (idx - n_sink);
+          const int pos = bf16_pos(sw, idx);
           rp = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
                            : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
         }
@@ -412,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(DecodeArgs a) {
         tmem_ld8(tl + kColQK + 64 * k + 16 * qd + h0, D);
         const uint32_t mw = meta[g * kTok + t];
         const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw));
-        const float centre = bf16_split ? centre_bf
+        const float centre = i >= n_pk ? centre_bf
                              : ((g < 8 && kTypeB) ? float(kCentre2) : float(kCentre4));
         const float s = sm.x, mp = fmaf(centre, sm.x, sm.y);
         const float4 qa = *reinterpret_cast<const float4*>(qsum + g * kHC + h0);

@@ -135,14 +135,19 @@ def test_write_decode_host_validation_without_launch():
 
 
 def _expected_splits(L, packed, chunk):
-    # Packed layouts: pages that hold at least one token served from packed codes
-    # (positions 4 .. L-129), cut into chunks, plus one split for the bf16 tokens.
+    # Work units of a sequence: for packed layouts the pages that hold at least
+    # one token served from packed codes (positions 4 .. L-129), then the
+    # protected tokens (sink 0..3 and recent L-128..L-1, each counted once) in
+    # 64-token tiles; for bf16 pages every page.  Splits cut the units into
+    # chunks, at least one split per sequence.
     if packed:
         served = [t for t in range(4, max(4, L - 128))]
         pages = len({t // 64 for t in served})
-        return math.ceil(pages / chunk) + 1
-    pages = math.ceil(L / 64)
-    return max(1, math.ceil(pages / chunk))
+        protected = len({t for t in range(L) if t < 4 or t >= L - 128})
+        units = pages + 3 * math.ceil(protected / 64)  # a bf16 tile counts 3 units
+    else:
+        units = math.ceil(L / 64)
+    return max(1, math.ceil(units / chunk))
 
 
 @pytest.mark.parametrize("cb", [4, 2, 16])
@@ -159,7 +164,8 @@ def test_plan_matches_definition(cb):
 
 
 def test_plan_fills_one_wave_on_uniform_lengths():
-    # one CTA per SM: the packed splits plus one bf16 split per sequence fit
-    # in a single wave of 152 CTAs
+    # one CTA per SM: 8 sequences of 510 packed-served pages + 3 protected-token
+    # tiles of 3 units each (519 units) -> 4,152 units in chunks of
+    # ceil(4152 / 152) = 28 -> 19 splits per sequence: one wave of 152 CTAs
     total, chunk, _ = pkg.decode_plan(pkg.layout(4, 4), 16, [32768] * 8, num_sms=152)
-    assert 152 - 16 <= total <= 152
+    assert (total, chunk) == (152, 28)
