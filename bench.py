@@ -233,6 +233,23 @@ class Setup:
         self.h_out.copy_(self.out, non_blocking=True)
 
 
+def reduce_max_over_ranks(values, dist, device):
+    """Element-wise max of per-rank values over all ranks (every rank gets the
+    result); the values themselves when there is one rank."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tokens_per_s(world: int, batch: int, t_ms: float) -> float:
+    """Output tokens of all ranks (one per sequence per step) per second, for a
+    step time that is already the max over ranks."""
+    return world * batch / (t_ms * 1e-3)
+
+
 def run_gpu(args, w):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -292,13 +309,10 @@ def run_gpu(args, w):
     t_step = sum(step_ms) / len(step_ms)
     t_dec = sum(dec_ms) / len(dec_ms)
     t_e2e = sum(e2e_ms) / len(e2e_ms)
-    if dist is not None:
-        t = torch.tensor([t_step, t_dec, t_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_dec, t_e2e = t.tolist()
+    t_step, t_dec, t_e2e = reduce_max_over_ranks([t_step, t_dec, t_e2e], dist, dev)
     B = w.batch
-    tokens_per_s = world * B / (t_step * 1e-3)
-    e2e_tokens_per_s = world * B / (t_e2e * 1e-3)
+    tokens_per_s = whole_job_tokens_per_s(world, B, t_step)
+    e2e_tokens_per_s = whole_job_tokens_per_s(world, B, t_e2e)
     by = algorithmic_bytes(w, s.lens)
     peak, peak_kind = peaks()
     step_bytes = by["decode"] + by["writer"]
