@@ -530,6 +530,51 @@ def run_table9(args):
                 torch.cuda.empty_cache()
 
 
+def run_mtp(args):
+    """Multi-token query decode on the v2lite shape (B8 H16 L32768 C4R4): decode
+    time for 1, 2 and 4 causal queries per sequence over the same cache (the
+    Group-Query Latent Attention abstract's s_q = 2 multi-token prediction
+    step). One JSON line per query count; L2 flushed before each timed call."""
+    import torch
+    w = syn.get("v2lite_c4r4")
+    s = Setup(w, "cuda:0")
+    peak, peak_kind = peaks()
+    tpk, tpk_kind = tensor_peak()
+    base = None
+    for n in (1, 2, 4):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(100 + n)
+        q = torch.randn(w.batch, n, w.heads, 576, generator=g, device="cuda").to(torch.bfloat16)
+        out = torch.empty(w.batch, n, w.heads, 512, dtype=torch.float32, device="cuda")
+        ws = s.cache.workspace(n * w.heads, s.lens_h)
+        for _ in range(3):
+            s.cache.decode_multi(q, s.lens_d, s.lens_h, w.softmax_scale, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.sweep_reps):
+            s.flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            s.cache.decode_multi(q, s.lens_d, s.lens_h, w.softmax_scale, out=out, workspace=ws)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        assert s.cache.error() == 0, f"device error word {s.cache.error()}"
+        med = sorted(ts)[len(ts) // 2]
+        base = base or med
+        by = algorithmic_bytes(w.with_(heads=n * w.heads), s.lens)["decode"]
+        fl = 2.0 * n * w.heads * (576 + 512) * float(np.sum(s.lens))
+        print(json.dumps({"sweep": "mtp", "workload": w.name, "queries_per_seq": n,
+                          "decode_us": round(med, 2), **{k: round(v, 2) for k, v in
+                                                         percentiles(ts).items()},
+                          "output_tokens_per_s": round(w.batch * n / (med * 1e-6), 1),
+                          "time_vs_one_query": round(med / base, 3),
+                          "hbm_frac": round(by / (med * 1e-6) / 1e9 / peak, 4),
+                          "tensor_frac": round(fl / (med * 1e-6) / 1e12 / tpk, 4),
+                          "peak_source": f"{peak_kind} hbm_gbs, {tpk_kind} bf16_tflops"}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,13 +584,17 @@ def main():
     ap.add_argument("--workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", choices=["table9"], default=None,
-                    help="context-length sweep instead of the benchmark line")
+    ap.add_argument("--sweep", choices=["table9", "mtp"], default=None,
+                    help="context-length sweep or multi-token query decode, instead of the "
+                         "benchmark line")
     ap.add_argument("--sweep-heads", type=int, default=16)
     ap.add_argument("--sweep-reps", type=int, default=15)
     args = ap.parse_args()
     if args.sweep == "table9":
         run_table9(args)
+        return
+    if args.sweep == "mtp":
+        run_mtp(args)
         return
     w = syn.get(args.workload)
     if args.impl == "reference":

@@ -27,6 +27,7 @@ EXPORTS = (
     "mla_lowbit_decode",
     "mla_lowbit_decode_noalloc",
     "mla_lowbit_write_decode",
+    "mla_lowbit_decode_multi",
     "mla_lowbit_read_error",
     "mla_lowbit_strerror",
     "mla_lowbit_version",
@@ -85,6 +86,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_lowbit_write_decode.argtypes = [lp, i32, i32, ctypes.c_float, vp, vp, vp, vp, i64, vp,
                                             i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.mla_lowbit_write_decode.restype = i32
+    lib.mla_lowbit_decode_multi.argtypes = [lp, i32, i32, i32, ctypes.c_float, vp, vp, i64, vp,
+                                            i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.mla_lowbit_decode_multi.restype = i32
     lib.mla_lowbit_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_lowbit_read_error.restype = i32
     lib.mla_lowbit_strerror.argtypes = [i32]
@@ -253,6 +257,37 @@ def write_decode(lay: Layout, q, ckv_new, krope_new, page_pool, block_table, seq
         _ptr(recent_buf), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
         _ptr(err_word), _stream(stream))
     _check(st, "mla_lowbit_write_decode")
+
+
+def decode_multi(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink_buf,
+                 recent_buf, out, workspace, err_word, softmax_scale: float, lse=None,
+                 stream=None):
+    """mla_lowbit_decode_multi: n causal queries per sequence, q [B][n][H][576]."""
+    torch = _torch()
+    B, n, H, _ = q.shape
+    _expect(q, "q", torch.bfloat16, (B, n, H, 576))
+    _expect(page_pool, "page_pool", torch.uint8)
+    _expect(block_table, "block_table", torch.int32)
+    _expect(seq_lens, "seq_lens", torch.int32, (B,))
+    _expect(out, "out", torch.float32, (B, n, H, 512))
+    _expect(workspace, "workspace", torch.uint8)
+    _expect(err_word, "err_word", torch.int32, (1,))
+    if lse is not None:
+        _expect(lse, "lse", torch.float32, (B, n, H))
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per sequence")
+    if lay.content_bits != 16:
+        _expect(sink_buf, "sink_buf", torch.bfloat16, (B, 4, 576))
+        _expect(recent_buf, "recent_buf", torch.bfloat16, (B, 128, 576))
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("seq_lens_host must have one entry per sequence")
+    st = load().mla_lowbit_decode_multi(
+        ctypes.byref(lay), B, n, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
+        page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream))
+    _check(st, "mla_lowbit_decode_multi")
 
 
 def decode_noalloc(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink_buf,

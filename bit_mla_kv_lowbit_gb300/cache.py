@@ -74,6 +74,20 @@ class PagedCache:
                              self.err, softmax_scale, lse=lse, stream=stream)
         return out
 
+    def decode_multi(self, q, seq_lens, seq_lens_host, softmax_scale: float, out=None, lse=None,
+                     workspace=None, stream=None):
+        """n causal queries per sequence (q [B][n][H][576]) over the cache."""
+        torch = self.torch
+        B, n, H, _ = q.shape
+        if out is None:
+            out = torch.empty(B, n, H, 512, dtype=torch.float32, device=self.device)
+        if workspace is None:
+            workspace = self.workspace(n * H, seq_lens_host)
+        binding.decode_multi(self.layout, q, self.pool, self.block_table, seq_lens, seq_lens_host,
+                             self.sink, self.recent, out, workspace, self.err, softmax_scale,
+                             lse=lse, stream=stream)
+        return out
+
     def error(self) -> int:
         return binding.read_error(self.err)
 

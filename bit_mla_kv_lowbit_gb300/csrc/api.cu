@@ -11,6 +11,8 @@ namespace mlalb {
 namespace {
 
 constexpr int kMaxHeads = 128;
+constexpr int kMaxQueries = 16;                    // queries per sequence (multi-query decode)
+constexpr int kMaxRows = kMaxHeads * kMaxQueries;  // rows of a sequence in a plan
 constexpr int kCtasPerSm = 1;
 constexpr long long kMaxChunkPages = 64;
 
@@ -98,7 +100,7 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
                            int* chunk_pages, size_t* workspace_bytes) {
   int st = check_layout(layout);
   if (st != MLA_LOWBIT_OK) return st;
-  if (num_seqs <= 0 || heads <= 0 || heads % 16 != 0 || heads > kMaxHeads) return MLA_LOWBIT_ESIZE;
+  if (num_seqs <= 0 || heads <= 0 || heads % 16 != 0 || heads > kMaxRows) return MLA_LOWBIT_ESIZE;
   if (!seq_lens_host || !total_splits || !chunk_pages || !workspace_bytes) return MLA_LOWBIT_ENULL;
   if (num_sms <= 0) num_sms = device_sm_count();
   if (num_sms <= 0) return MLA_LOWBIT_ECUDA;
@@ -131,7 +133,7 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
 // Decode, optionally appending one token per sequence first (ckv_new and
 // krope_new non-null): fused into the decode launch when the split kernel
 // supports it, else the writer kernel runs first on the same stream.
-static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int heads,
+static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, int heads,
                        float softmax_scale, const void* q, const void* ckv_new,
                        const void* krope_new, void* page_pool, int64_t num_pages,
                        const int32_t* block_table, int max_pages, const int32_t* seq_lens,
@@ -141,7 +143,7 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int heads,
   int st = check_layout(layout);
   if (st != MLA_LOWBIT_OK) return st;
   if (num_seqs <= 0 || heads <= 0 || heads % 16 != 0 || heads > kMaxHeads || max_pages <= 0 ||
-      num_pages <= 0)
+      num_pages <= 0 || n_q < 1 || n_q > kMaxQueries)
     return MLA_LOWBIT_ESIZE;
   if ((long long)max_pages * kPageTokens > INT32_MAX) return MLA_LOWBIT_ESIZE;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MLA_LOWBIT_EINVAL;
@@ -160,14 +162,16 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int heads,
     if (seq_lens_host[b] < 0 || (long long)seq_lens_host[b] > (long long)max_pages * kPageTokens)
       return MLA_LOWBIT_EINVAL;
     if (append && seq_lens_host[b] < 1) return MLA_LOWBIT_EINVAL;
+    if (n_q > 1 && seq_lens_host[b] < n_q) return MLA_LOWBIT_EINVAL;  // queries' tokens cached
   }
+  const int rows = n_q * heads;  // rows of a sequence: n_q blocks of `heads`
   int total = 0, chunk = 0;
   size_t need = 0;
-  st = mla_lowbit_decode_plan(layout, num_seqs, heads, seq_lens_host, 0, &total, &chunk, &need);
+  st = mla_lowbit_decode_plan(layout, num_seqs, rows, seq_lens_host, 0, &total, &chunk, &need);
   if (st != MLA_LOWBIT_OK) return st;
   if (workspace_bytes < need) return MLA_LOWBIT_EWORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool fused = append && decode_fuses_append(layout->content_bits);
+  const bool fused = append && n_q == 1 && decode_fuses_append(layout->content_bits);
   if (append && !fused) {
     WriterArgs w;
     w.ckv = static_cast<const uint32_t*>(ckv_new);
@@ -195,11 +199,12 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int heads,
   a.sink = static_cast<const uint16_t*>(sink_buf);
   a.recent = static_cast<const uint16_t*>(recent_buf);
   a.part_o = static_cast<float*>(workspace);
-  a.part_ml = a.part_o + (size_t)total * heads * kLatent;
-  a.seq_split = reinterpret_cast<int32_t*>(a.part_ml + (size_t)total * heads * 2);
+  a.part_ml = a.part_o + (size_t)total * rows * kLatent;
+  a.seq_split = reinterpret_cast<int32_t*>(a.part_ml + (size_t)total * rows * 2);
   a.err = err_word;
   a.B = num_seqs;
-  a.H = heads;
+  a.H = rows;
+  a.n_q = n_q;
   a.max_pages = max_pages;
   a.chunk_pages = chunk;
   a.total_splits = total;
@@ -222,7 +227,7 @@ int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
                       const void* sink_buf, const void* recent_buf, float* out, float* lse,
                       void* workspace, size_t workspace_bytes, int32_t* err_word,
                       void* stream) {
-  return decode_impl(layout, num_seqs, heads, softmax_scale, q, nullptr, nullptr,
+  return decode_impl(layout, num_seqs, 1, heads, softmax_scale, q, nullptr, nullptr,
                      const_cast<void*>(page_pool), num_pages, block_table, max_pages, seq_lens,
                      seq_lens_host, const_cast<void*>(sink_buf), const_cast<void*>(recent_buf), out,
                      lse, workspace, workspace_bytes, err_word, stream);
@@ -236,9 +241,22 @@ int mla_lowbit_write_decode(const mla_lowbit_layout* layout, int num_seqs, int h
                             float* out, float* lse, void* workspace, size_t workspace_bytes,
                             int32_t* err_word, void* stream) {
   if (!ckv_new || !krope_new) return MLA_LOWBIT_ENULL;
-  return decode_impl(layout, num_seqs, heads, softmax_scale, q, ckv_new, krope_new, page_pool,
+  return decode_impl(layout, num_seqs, 1, heads, softmax_scale, q, ckv_new, krope_new, page_pool,
                      num_pages, block_table, max_pages, seq_lens, seq_lens_host, sink_buf,
                      recent_buf, out, lse, workspace, workspace_bytes, err_word, stream);
+}
+
+int mla_lowbit_decode_multi(const mla_lowbit_layout* layout, int num_seqs, int queries_per_seq,
+                            int heads, float softmax_scale, const void* q, const void* page_pool,
+                            int64_t num_pages, const int32_t* block_table, int max_pages,
+                            const int32_t* seq_lens, const int32_t* seq_lens_host,
+                            const void* sink_buf, const void* recent_buf, float* out, float* lse,
+                            void* workspace, size_t workspace_bytes, int32_t* err_word,
+                            void* stream) {
+  return decode_impl(layout, num_seqs, queries_per_seq, heads, softmax_scale, q, nullptr, nullptr,
+                     const_cast<void*>(page_pool), num_pages, block_table, max_pages, seq_lens,
+                     seq_lens_host, const_cast<void*>(sink_buf), const_cast<void*>(recent_buf), out,
+                     lse, workspace, workspace_bytes, err_word, stream);
 }
 
 int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out) {

@@ -156,6 +156,9 @@ struct DecodeArgs {
   int32_t* err;
   int B, H, max_pages, chunk_pages, total_splits;
   float scale_log2;  // softmax_scale * log2(e)
+  // Queries per sequence: the H rows of a sequence are n_q blocks of H / n_q
+  // heads, query i at position seq_lens[b] - n_q + i (causal among them).
+  int n_q = 1;
   // Fused append (mla_lowbit_write_decode): the token at position
   // seq_lens[b] - 1 of every sequence, written by the sequence's bf16 split of
   // head chunk 0 and read from here by every bf16 split.  Null for a plain decode.

@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   }
   const int valid_lo = kPacked ? kSink : 0;
   const int valid_hi = kPacked ? L - kLocal : L;  // packed-served tokens [lo, hi)
+  // query blocks: this head chunk's query does not see the sequence's last
+  // n_masked tokens (all inside the recent window)
+  const int n_masked = a.n_q - 1 - (hc * kHC) / (a.H / a.n_q);
 
   // Copy packed page `tile_i` of this split into the team's staging buffer.
   auto stage_page = [&](int tile_i) {
@@ -342,8 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
                                  : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
           }
         }
-        v0 = bt * kPageTokens + tC0 < sw.n_tok;
-        v1 = bt * kPageTokens + tC0 + 1 < sw.n_tok;
+        // the protected-token list is in position order: the masked tokens are
+        // its last n_masked entries
+        const int visible = sw.n_tok - n_masked;
+        v0 = bt * kPageTokens + tC0 < visible;
+        v1 = bt * kPageTokens + tC0 + 1 < visible;
       } else {
         const int page_idx = page_begin + tile_i;
         const long long page = a.block_table[(long long)b * a.max_pages + page_idx];
@@ -352,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
         const int tok0 = page_idx * kPageTokens;
         if (page_ok)
           rowptr = reinterpret_cast<const uint16_t*>(a.pool + page * G.page_bytes) + rowB * kDim;
-        v0 = page_ok && tok0 + tC0 < L;
-        v1 = page_ok && tok0 + tC0 + 1 < L;
+        v0 = page_ok && tok0 + tC0 < L - n_masked;
+        v1 = page_ok && tok0 + tC0 + 1 < L - n_masked;
       }
 #pragma unroll 1
       for (int g = 0; g < kGroups; ++g) {
@@ -662,8 +668,8 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
 // layouts, the hybrid mma.sync + tcgen05 kernel ("hy", decode_hy.cu) or the
 // all-tcgen05 kernel ("tc", decode_tc.cu).
 enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp };
-static SplitKernel split_kernel(int cbits) {
-  if (cbits == 16) return SplitKernel::kMma;
+static SplitKernel split_kernel(int cbits, int n_q = 1) {
+  if (cbits == 16 || n_q > 1) return SplitKernel::kMma;  // the only one with query blocks
   const char* v = getenv("MLA_LOWBIT_DECODE");
   if (v && v[0] == 'h') return SplitKernel::kHybrid;
   if (v && v[0] == 't') return SplitKernel::kTc;
@@ -677,7 +683,7 @@ bool decode_fuses_append(int cbits) {
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream) {
-  const SplitKernel sk = split_kernel(cbits);
+  const SplitKernel sk = split_kernel(cbits, a.n_q);
   if (sk != SplitKernel::kMma) {
     cudaError_t et = sk == SplitKernel::kTc     ? launch_decode_tc(cbits, a, stream)
                      : sk == SplitKernel::kHybrid ? launch_decode_hy(cbits, a, stream)

@@ -148,7 +148,9 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
  *   z_t    = softmax_scale * dot(q[s][h][0:576], key_t[0:576]);
  *   out[s][h][c] = sum_t softmax(z)_t * key_t[c],  c < 512 (value = latent);
  *   lse[s][h]    = log(sum_t exp(z_t)) (natural log; -inf and out = 0 when L = 0).
- * heads must be a multiple of 16, at most 128.
+ * heads must be a multiple of 16, at most 128 (mla_lowbit_decode_plan takes
+ * the rows of a sequence: heads, or n * heads for mla_lowbit_decode_multi,
+ * at most 2048).
  *
  *   q             [num_seqs][heads][576] bf16
  *   page_pool     [num_pages][page_bytes] u8 (as written by mla_lowbit_write)
@@ -198,6 +200,27 @@ int mla_lowbit_write_decode(const mla_lowbit_layout* layout, int num_seqs, int h
                             const int32_t* seq_lens_host, void* sink_buf, void* recent_buf,
                             float* out, float* lse, void* workspace, size_t workspace_bytes,
                             int32_t* err_word, void* stream);
+
+/* Multi-token query decode (several new tokens per sequence at once, as for
+ * multi-token prediction or speculative verification): queries_per_seq = n
+ * queries per sequence at positions L - n .. L - 1 (L = seq_lens[s], all n
+ * tokens already written), each attending causally: query i sees tokens
+ * 0 .. L - n + i.  Same arithmetic, tolerance and errors as mla_lowbit_decode
+ * otherwise; the n queries run as n blocks of `heads` rows over one pass of the
+ * cache (the masked tokens are all inside the recent window, 1 <= n <= 16).
+ *
+ *   q      [num_seqs][n][heads][576] bf16
+ *   out    [num_seqs][n][heads][512] float32; lse [num_seqs][n][heads] or NULL
+ *   seq_lens_host entries >= n
+ *   workspace  mla_lowbit_decode_plan with heads = n * heads
+ * Always runs on the mma.sync split kernel. */
+int mla_lowbit_decode_multi(const mla_lowbit_layout* layout, int num_seqs, int queries_per_seq,
+                            int heads, float softmax_scale, const void* q, const void* page_pool,
+                            int64_t num_pages, const int32_t* block_table, int max_pages,
+                            const int32_t* seq_lens, const int32_t* seq_lens_host,
+                            const void* sink_buf, const void* recent_buf, float* out, float* lse,
+                            void* workspace, size_t workspace_bytes, int32_t* err_word,
+                            void* stream);
 
 /* mla_lowbit_decode for callers that cannot allocate device memory.  The
  * pages have no counterpart to this entry point: it exists because some hosts

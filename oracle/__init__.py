@@ -28,4 +28,4 @@ from .quant import (  # noqa: F401
 )
 from .layout import Layout, bytes_per_token, compression_ratio, page_geometry  # noqa: F401
 from .cache import PagedCacheModel, is_protected, reference_keys  # noqa: F401
-from .attention import mla_decode_fp64  # noqa: F401
+from .attention import mla_decode_fp64, mla_decode_multi_fp64  # noqa: F401

@@ -40,3 +40,29 @@ def mla_decode_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float):
     out = (e @ keys[:, :512]) / denom[:, None]
     lse = zmax[:, 0] + np.log(denom)
     return out, lse
+
+
+def mla_decode_multi_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float):
+    """Several queries of one sequence decoded in one step, causally.
+
+    Group-Query Latent Attention abstract (Shi, Meng, Zhang): multi-token
+    prediction decodes s_q = 2 query tokens per step on the same latent cache
+    that the absorbed path reads with s_q = 1.  Adopted reading: the ``n``
+    queries are the sequence's last ``n`` tokens (positions ``L - n .. L - 1``,
+    all already cached), and query ``i`` attends to the tokens up to and
+    including its own position, ``keys[: L - n + i + 1]`` -- ordinary causal
+    attention, each query exactly ``mla_decode_fp64`` over its prefix.
+
+    ``q_bits``: bf16 bits ``[n][H][576]``; ``keys``: float64 ``[L][576]``
+    with ``L >= n``.  Returns ``(out [n][H][512], lse [n][H])``.
+    """
+    q_bits = np.asarray(q_bits)
+    n = q_bits.shape[0]
+    L = np.asarray(keys).shape[0]
+    assert L >= n, "the queries' own tokens must be cached"
+    outs, lses = [], []
+    for i in range(n):
+        o, l = mla_decode_fp64(q_bits[i], np.asarray(keys)[: L - n + i + 1], softmax_scale)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)

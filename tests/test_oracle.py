@@ -213,6 +213,49 @@ def test_one_hot_logit_selects_one_token():
     assert np.abs(out - keys[star, :512][None]).max() <= bound + 1e-13
 
 
+def test_multi_query_causal_boundary_selects_own_token():
+    # Logits grow by 0.25 * 1024 * scale per position (key channel 512 = t / 4),
+    # so every query's softmax concentrates on the latest token it may see:
+    # query i of n sits at position L - n + i and must select exactly that
+    # token (seeing one more, or one fewer, would select a neighbour).
+    L, n = 300, 4
+    rng = np.random.default_rng(11)
+    keys = rng.standard_normal((L, 576))
+    keys[:, 512:] = 0.0
+    keys[:, 512] = np.arange(L) / 4.0
+    q = np.zeros((n, 3, 576), np.float32)
+    q[:, :, 512] = 1024.0
+    scale = 1 / math.sqrt(192)
+    out, lse = oracle.mla_decode_multi_fp64(bf16(q.reshape(n * 3, 576)).reshape(n, 3, 576),
+                                            keys, scale)
+    gap = scale * 1024.0 * 0.25
+    assert gap > 18
+    for i in range(n):
+        own = L - n + i
+        bound = 2 * math.exp(-gap) * np.abs(keys[:, :512]).max() / (1 - math.exp(-gap))
+        assert np.abs(out[i] - keys[own, :512][None]).max() <= bound
+        # lse is the log of the visible tokens' exp(logit): dominated by the own token
+        assert abs(lse[i, 0] - scale * 1024.0 * keys[own, 512]) < 1e-6
+
+
+def test_multi_query_matches_masked_torch_sdpa():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    L, n, H = 40, 3, 2
+    keys = rng.standard_normal((L, 576))
+    q = bf16(rng.standard_normal((n * H, 576)) * 0.3).reshape(n, H, 576)
+    scale = 0.05
+    out, _ = oracle.mla_decode_multi_fp64(q, keys, scale)
+    qf = torch.from_numpy(syn.f32_from_bf16_bits(q).astype(np.float64))      # [n][H][576]
+    k = torch.from_numpy(keys)                                               # [L][576]
+    # MQA layout: heads as the batch, queries as the sequence; explicit mask
+    mask = torch.tensor([[t <= L - n + i for t in range(L)] for i in range(n)])
+    got = torch.nn.functional.scaled_dot_product_attention(
+        qf.permute(1, 0, 2), k[None].expand(H, L, 576), k[None, :, :512].expand(H, L, 512),
+        attn_mask=mask, scale=scale).permute(1, 0, 2).numpy()
+    assert np.abs(got - out).max() < 1e-12
+
+
 def test_bruteforce_tiny_softmax_without_max_subtraction():
     rng = np.random.default_rng(5)
     for L in (1, 2, 5, 8):
