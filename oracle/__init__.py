@@ -25,6 +25,9 @@ from .quant import (  # noqa: F401
     quantize_group,
     quantize_token,
     unpack_codes,
+    hadamard_matrix64,
+    hadamard_rotate_f32,
+    rotate_latent_bits,
 )
 from .layout import Layout, bytes_per_token, compression_ratio, page_geometry  # noqa: F401
 from .cache import PagedCacheModel, is_protected, reference_keys  # noqa: F401

@@ -16,16 +16,29 @@ from __future__ import annotations
 
 import numpy as np
 
-from .quant import bf16_bits_to_f64
+from .quant import bf16_bits_to_f64, hadamard_matrix64
 
 
-def mla_decode_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float):
+def _rotate_groups(x: np.ndarray) -> np.ndarray:
+    """R applied to each 64-channel group of ``[..., 512]`` (float64, R = R^T)."""
+    R = hadamard_matrix64()
+    lead = x.shape[:-1]
+    return (x.reshape(lead + (8, 64)) @ R.T).reshape(lead + (512,))
+
+
+def mla_decode_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float,
+                    rotate: bool = False):
     """Softmax attention of ``H`` heads over ``L`` keys.
 
     ``q_bits``: bf16 bits ``[H][576]``; ``keys``: float64 ``[L][576]``.
     Returns ``(out [H][512] float64, lse [H] float64)`` where ``lse`` is the
     natural-log sum of ``exp(logit)``.  With ``L == 0`` the output is zero and
     ``lse`` is ``-inf``.
+
+    ``rotate``: the keys' content channels are in the rotated basis of an
+    online-rotated cache (``quant.rotate_latent_bits``); the query's content
+    channels are rotated by the same R and the output rotated back, so the
+    logits are ``q . R^T k'`` and the output ``R^T sum p k'``.
     """
     q = bf16_bits_to_f64(q_bits)
     keys = np.asarray(keys, dtype=np.float64)
@@ -33,16 +46,22 @@ def mla_decode_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float):
     L = keys.shape[0]
     if L == 0:
         return np.zeros((H, 512)), np.full(H, -np.inf)
+    if rotate:
+        q = q.copy()
+        q[:, :512] = _rotate_groups(q[:, :512])
     z = float(softmax_scale) * (q @ keys.T)          # [H][L]
     zmax = z.max(axis=1, keepdims=True)
     e = np.exp(z - zmax)
     denom = e.sum(axis=1)
     out = (e @ keys[:, :512]) / denom[:, None]
+    if rotate:
+        out = _rotate_groups(out)
     lse = zmax[:, 0] + np.log(denom)
     return out, lse
 
 
-def mla_decode_multi_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float):
+def mla_decode_multi_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: float,
+                          rotate: bool = False):
     """Several queries of one sequence decoded in one step, causally.
 
     Group-Query Latent Attention abstract (Shi, Meng, Zhang): multi-token
@@ -62,7 +81,8 @@ def mla_decode_multi_fp64(q_bits: np.ndarray, keys: np.ndarray, softmax_scale: f
     assert L >= n, "the queries' own tokens must be cached"
     outs, lses = [], []
     for i in range(n):
-        o, l = mla_decode_fp64(q_bits[i], np.asarray(keys)[: L - n + i + 1], softmax_scale)
+        o, l = mla_decode_fp64(q_bits[i], np.asarray(keys)[: L - n + i + 1], softmax_scale,
+                               rotate=rotate)
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)

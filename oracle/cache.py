@@ -27,7 +27,8 @@ from __future__ import annotations
 import numpy as np
 
 from .layout import LATENT, LOCAL, PAGE_TOKENS, ROPE, SINK, Layout, page_geometry
-from .quant import bf16_bits_to_f64, dequantize, pack_codes, quantize_token, unpack_codes
+from .quant import (bf16_bits_to_f64, dequantize, pack_codes, quantize_token, rotate_latent_bits,
+                    unpack_codes)
 
 
 def is_protected(t: np.ndarray, L: int) -> np.ndarray:
@@ -67,6 +68,9 @@ class PagedCacheModel:
         page, row = self._rows(seq, pos)
         g = self.geom
         lay = self.layout
+        if lay.rotate:
+            # the token is stored (packed and bf16 copies alike) in the rotated basis
+            ckv_bits = rotate_latent_bits(ckv_bits)
         if lay.packed:
             cc, rc, s16, m16 = quantize_token(ckv_bits, krope_bits, lay.content_bits,
                                               lay.rope_bits)

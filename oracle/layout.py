@@ -30,11 +30,14 @@ N_GROUPS = (LATENT + ROPE) // GROUP  # 8 content + 1 rope
 class Layout:
     content_bits: int = 4   # 4, 2 or 16 (bf16 pages)
     rope_bits: int = 4      # 4, or 16 with bf16 pages
+    rotate: bool = False    # online Hadamard rotation of the content latent (packed only)
 
     def __post_init__(self):
         ok = (self.content_bits, self.rope_bits) in ((4, 4), (2, 4), (16, 16))
         if not ok:
             raise ValueError(f"unsupported layout C{self.content_bits}R{self.rope_bits}")
+        if self.rotate and not self.packed:
+            raise ValueError("rotation applies to packed layouts")
 
     @property
     def packed(self) -> bool:

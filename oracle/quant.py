@@ -114,3 +114,51 @@ def dequantize(codes: np.ndarray, scale16: np.ndarray, min16: np.ndarray) -> np.
     s = scale16.astype(np.float64)[..., None]
     m = min16.astype(np.float64)[..., None]
     return (s * g + m).reshape(lead + (n,))
+
+
+# ---------------------------------------------------------------- online rotation
+# QuaRot-style online rotation of the content latent (QuantMLA, Table 1: QuaRot
+# as an MLA-adapted baseline; the pages' own transforms are fused offline).
+# Adopted reading for an un-fused model: each 64-channel content group x is
+# replaced, as it is written, by R x with R = H_64 / 8 the orthonormal
+# Sylvester-Hadamard matrix (R symmetric, R R = I), computed in float32 and
+# rounded to bf16; queries are rotated the same way and attention outputs
+# rotated back, so attention sees the same inner products.  RoPE keys are not
+# rotated.
+
+def hadamard_matrix64() -> np.ndarray:
+    """R = H_64 / 8 in float64: R[i][j] = (-1)^popcount(i & j) / 8."""
+    i = np.arange(64)
+    pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1.0, -1.0) / 8.0
+
+
+def hadamard_rotate_f32(x: np.ndarray) -> np.ndarray:
+    """R x for groups of 64 along the last axis, in float32 with a fixed order of
+    operations: butterfly stages h = 1, 2, 4, ..., 32, where element i (bit h
+    clear) and element i + h become (a + b, a - b); then a scale by 1/8 (exact)."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    h = 1
+    while h < 64:
+        lo = np.array([i for i in range(64) if not i & h])
+        a = y[..., lo].copy()
+        b = y[..., lo + h].copy()
+        y[..., lo] = a + b
+        y[..., lo + h] = a - b
+        h *= 2
+    return y * np.float32(0.125)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even); finite inputs only."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def rotate_latent_bits(ckv_bits: np.ndarray) -> np.ndarray:
+    """The rotated content latent as bf16 bits: the 8 groups of ``[..., 512]``
+    each rotated by R (float32) and rounded to bf16."""
+    x = bf16_bits_to_f32(ckv_bits)
+    lead = x.shape[:-1]
+    y = hadamard_rotate_f32(x.reshape(lead + (8, 64))).reshape(lead + (512,))
+    return f32_to_bf16_bits(y)

@@ -256,6 +256,60 @@ def test_multi_query_matches_masked_torch_sdpa():
     assert np.abs(got - out).max() < 1e-12
 
 
+def test_hadamard_rotation_closed_forms():
+    R = oracle.hadamard_matrix64()
+    # orthonormal and symmetric: R R = I
+    assert np.array_equal(R @ R, np.eye(64)) and np.array_equal(R, R.T)
+    # the butterfly on e_k is column k of R, exactly (entries +-1/8)
+    eye = np.eye(64, dtype=np.float32)
+    assert np.array_equal(oracle.hadamard_rotate_f32(eye), R.T.astype(np.float32))
+    # small integers: every partial sum is exact in float32
+    rng = np.random.default_rng(21)
+    xi = rng.integers(-1000, 1000, size=(50, 64)).astype(np.float32)
+    assert np.array_equal(oracle.hadamard_rotate_f32(xi).astype(np.float64), xi.astype(np.float64) @ R.T)
+    # bf16 inputs: within float32 rounding of six butterfly stages
+    xb = syn.f32_from_bf16_bits(bf16(rng.standard_normal((50, 64)) * 10)).astype(np.float32)
+    want = xb.astype(np.float64) @ R.T
+    err = np.abs(oracle.hadamard_rotate_f32(xb).astype(np.float64) - want)
+    assert np.all(err <= 6 * 2.0 ** -24 * np.abs(xb).astype(np.float64).sum(axis=1, keepdims=True))
+
+
+def test_rotated_attention_equals_unrotated_on_exact_keys():
+    # keys stored in the rotated basis (exactly, in float64) must give the same
+    # logits and outputs as the plain keys: q is rotated, the output rotated back
+    rng = np.random.default_rng(22)
+    L, H = 60, 3
+    keys = rng.standard_normal((L, 576)) * 3
+    R = oracle.hadamard_matrix64()
+    rk = keys.copy()
+    rk[:, :512] = (keys[:, :512].reshape(L, 8, 64) @ R.T).reshape(L, 512)
+    q = bf16(rng.standard_normal((H, 576)))
+    o0, l0 = oracle.mla_decode_fp64(q, keys, 0.05)
+    o1, l1 = oracle.mla_decode_fp64(q, rk, 0.05, rotate=True)
+    assert np.abs(o0 - o1).max() < 1e-12 and np.abs(l0 - l1).max() < 1e-12
+
+
+def test_rotated_cache_stores_the_rotated_latent():
+    L = 200
+    ckv, kr = _tokens(L, 4)
+    lay = oracle.Layout(4, 4, rotate=True)
+    table = np.arange(4, dtype=np.int32)[None, :]
+    m = oracle.PagedCacheModel(lay, 4, table)
+    m.write(np.zeros(L, np.int64), np.arange(L), ckv, kr, np.array([L]))
+    rot = oracle.rotate_latent_bits(ckv)
+    # bf16 copies (sink and ring) hold the rotated latent and the unrotated RoPE key
+    assert np.array_equal(m.sink[0, :4, :512], rot[:4])
+    assert np.array_equal(m.recent[0, np.arange(L - 128, L) % 128, :512], rot[L - 128:])
+    assert np.array_equal(m.recent[0, np.arange(L - 128, L) % 128, 512:], kr[L - 128:])
+    # packed codes are those of the rotated latent: same bytes as an unrotated
+    # cache fed the rotated bits
+    plain = oracle.PagedCacheModel(oracle.Layout(4, 4), 4, table)
+    plain.write(np.zeros(L, np.int64), np.arange(L), rot, kr, np.array([L]))
+    assert np.array_equal(m.pool, plain.pool)
+    with pytest.raises(ValueError):
+        oracle.Layout(16, 16, rotate=True)
+
+
 def test_bruteforce_tiny_softmax_without_max_subtraction():
     rng = np.random.default_rng(5)
     for L in (1, 2, 5, 8):
