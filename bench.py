@@ -167,7 +167,7 @@ def traffic_record(kernel_key: str):
 # ---------------------------------------------------------------- the GPU arm
 
 class Setup:
-    def __init__(self, w: syn.Workload, dev: str):
+    def __init__(self, w: syn.Workload, dev: str, rotate: bool = False):
         import torch
         import bit_mla_kv_lowbit_gb300 as pkg
         self.torch = torch
@@ -175,7 +175,8 @@ class Setup:
         self.dev = dev
         self.lens = syn.sequence_lengths(w).astype(np.int32)
         self.table, self.npages = syn.make_paging(w)
-        self.cache = pkg.PagedCache(w.content_bits, w.rope_bits, self.table, self.npages, dev)
+        self.cache = pkg.PagedCache(w.content_bits, w.rope_bits, self.table, self.npages, dev,
+                                    rotate=rotate)
         scales = syn.channel_scales(w)
         B = w.batch
         new_ckv = np.empty((B, 512), np.uint16)
@@ -575,6 +576,40 @@ def run_mtp(args):
               flush=True)
 
 
+def run_rotate(args):
+    """Cost of the online Hadamard rotation: the write + decode step (one
+    mla_lowbit_write_decode call) on the same workload with a plain and a
+    rotated cache.  One JSON line per (workload, rotation); L2 flushed before
+    each timed call."""
+    import torch
+    v2 = syn.get("v2lite_c4r4")
+    for w in (v2, v2.with_(name="v2lite_c2r4", content_bits=2)):
+        base = None
+        for rot in (False, True):
+            s = Setup(w, "cuda:0", rotate=rot)
+            for _ in range(3):
+                s.step()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(args.sweep_reps):
+                s.flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                s.step()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            assert s.cache.error() == 0, f"device error word {s.cache.error()}"
+            med = sorted(ts)[len(ts) // 2]
+            base = base or med
+            print(json.dumps({"sweep": "rotate", "workload": w.name, "rotate": rot,
+                              "step_us": round(med, 2),
+                              **{k: round(v, 2) for k, v in percentiles(ts).items()},
+                              "time_vs_plain": round(med / base, 3)}), flush=True)
+            del s
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -584,9 +619,9 @@ def main():
     ap.add_argument("--workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", choices=["table9", "mtp"], default=None,
-                    help="context-length sweep or multi-token query decode, instead of the "
-                         "benchmark line")
+    ap.add_argument("--sweep", choices=["table9", "mtp", "rotate"], default=None,
+                    help="context-length sweep, multi-token query decode or the cost of the "
+                         "online rotation, instead of the benchmark line")
     ap.add_argument("--sweep-heads", type=int, default=16)
     ap.add_argument("--sweep-reps", type=int, default=15)
     args = ap.parse_args()
@@ -595,6 +630,9 @@ def main():
         return
     if args.sweep == "mtp":
         run_mtp(args)
+        return
+    if args.sweep == "rotate":
+        run_rotate(args)
         return
     w = syn.get(args.workload)
     if args.impl == "reference":

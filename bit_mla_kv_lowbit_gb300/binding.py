@@ -39,11 +39,11 @@ DEV_BAD_SEQ, DEV_BAD_POS, DEV_BAD_PAGE, DEV_BAD_LEN, DEV_PLAN, DEV_PIPELINE = 1,
 class Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("content_bits", "rope_bits", "group", "sink", "local", "page_tokens",
-                 "latent", "rope")]
+                 "latent", "rope", "rotate")]
 
 
-def layout(content_bits: int = 4, rope_bits: int = 4) -> Layout:
-    return Layout(content_bits, rope_bits, 64, 4, 128, 64, 512, 64)
+def layout(content_bits: int = 4, rope_bits: int = 4, rotate: bool = False) -> Layout:
+    return Layout(content_bits, rope_bits, 64, 4, 128, 64, 512, 64, int(bool(rotate)))
 
 
 class LibraryError(RuntimeError):

@@ -17,10 +17,10 @@ class PagedCache:
     """Page pool, bf16 sink/recent buffers, block table and device error word."""
 
     def __init__(self, content_bits: int, rope_bits: int, block_table, num_pages: int,
-                 device: str = "cuda"):
+                 device: str = "cuda", rotate: bool = False):
         import torch
         self.torch = torch
-        self.layout = binding.layout(content_bits, rope_bits)
+        self.layout = binding.layout(content_bits, rope_bits, rotate)
         self.page_bytes = binding.page_bytes(self.layout)
         bt = torch.as_tensor(np.asarray(block_table, dtype=np.int32))
         self.block_table = bt.to(device).contiguous()

@@ -24,6 +24,7 @@ int check_layout(const mla_lowbit_layout* l) {
   if (!ok_bits || l->group != kGroup || l->sink != kSink || l->local != kLocal ||
       l->page_tokens != kPageTokens || l->latent != kLatent || l->rope != kRope)
     return MLA_LOWBIT_EINVAL;
+  if (l->rotate != 0 && (l->rotate != 1 || l->content_bits == 16)) return MLA_LOWBIT_EINVAL;
   return MLA_LOWBIT_OK;
 }
 
@@ -91,6 +92,7 @@ int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* 
   a.n_tokens = n_tokens;
   a.num_seqs = num_seqs;
   a.max_pages = max_pages;
+  a.rotate = layout->rotate;
   cudaError_t e = launch_writer(layout->content_bits, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_LOWBIT_OK : MLA_LOWBIT_ECUDA;
 }
@@ -171,7 +173,9 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, i
   if (st != MLA_LOWBIT_OK) return st;
   if (workspace_bytes < need) return MLA_LOWBIT_EWORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool fused = append && n_q == 1 && decode_fuses_append(layout->content_bits);
+  // the fused append reads the new token's unrotated input: not with rotation
+  const bool fused = append && n_q == 1 && !layout->rotate &&
+                     decode_fuses_append(layout->content_bits);
   if (append && !fused) {
     WriterArgs w;
     w.ckv = static_cast<const uint32_t*>(ckv_new);
@@ -188,6 +192,7 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, i
     w.n_tokens = num_seqs;
     w.num_seqs = num_seqs;
     w.max_pages = max_pages;
+    w.rotate = layout->rotate;
     if (launch_writer(layout->content_bits, w, s) != cudaSuccess) return MLA_LOWBIT_ECUDA;
   }
   DecodeArgs a;
@@ -205,6 +210,7 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, i
   a.B = num_seqs;
   a.H = rows;
   a.n_q = n_q;
+  a.rotate = layout->rotate;
   a.max_pages = max_pages;
   a.chunk_pages = chunk;
   a.total_splits = total;

@@ -140,6 +140,7 @@ struct WriterArgs {
   int32_t* err;
   long long num_pages;
   int n_tokens, num_seqs, max_pages;
+  int rotate = 0;  // online Hadamard rotation of the content latent (layout field)
 };
 
 struct DecodeArgs {
@@ -159,6 +160,7 @@ struct DecodeArgs {
   // Queries per sequence: the H rows of a sequence are n_q blocks of H / n_q
   // heads, query i at position seq_lens[b] - n_q + i (causal among them).
   int n_q = 1;
+  int rotate = 0;  // the cache's content latent is stored rotated (layout field)
   // Fused append (mla_lowbit_write_decode): the token at position
   // seq_lens[b] - 1 of every sequence, written by the sequence's bf16 split of
   // head chunk 0 and read from here by every bf16 split.  Null for a plain decode.

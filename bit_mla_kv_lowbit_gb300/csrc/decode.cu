@@ -43,7 +43,8 @@ constexpr int kQStride = kDim + 8;      // fp16 per q row in shared memory
 constexpr int kPStride = 72;            // floats per P row
 // shared by both teams
 constexpr int kOffQ = 0;
-constexpr int kOffQsum = kOffQ + kHC * kQStride * 2;
+constexpr int kQBytes = kHC * kQStride * 2;
+constexpr int kOffQsum = kOffQ + kQBytes;
 constexpr int kOffScan = kOffQsum + kGroups * kHC * 4;
 constexpr int kOffPages = kOffScan + 64 * 4;  // [64] page ids of the split
 constexpr int kOffTeam = ((kOffPages + 64 * 4) + 127) / 128 * 128;
@@ -57,8 +58,11 @@ constexpr int kTOffStage = kTOffMax + kTeamWarps * kHC * 4;
 __host__ __device__ constexpr int team_bytes(int cbits) {
   return kTOffStage + (cbits == 16 ? 0 : page_geom(cbits).page_bytes);
 }
-__host__ __device__ constexpr int smem_bytes(int cbits) { return kOffTeam + kTeams * team_bytes(cbits); }
-static_assert(smem_bytes(4) <= 227 * 1024, "shared memory budget");
+// a rotated q keeps its low fp16 parts after the two teams
+__host__ __device__ constexpr int smem_bytes(int cbits, bool rot = false) {
+  return kOffTeam + kTeams * team_bytes(cbits) + (rot ? kQBytes : 0);
+}
+static_assert(smem_bytes(4, true) <= 227 * 1024, "shared memory budget");
 
 // ---------------------------------------------------------------- split kernel
 __device__ __forceinline__ void team_sync(int team) {
@@ -87,13 +91,18 @@ __device__ __forceinline__ int stage_swizzle(int r) {
 // of 8 warps take alternate pages of the split, each with its own running max,
 // sum and output, and merge at the end.  Packed pages are copied into a
 // per-team staging buffer with cp.async one page ahead.
-template <int CB>
+// kRot: the cache holds the online-rotated content latent; q's content groups
+// are rotated here (float32) and kept as fp16 high + low parts, so QK runs a
+// second MMA per content k-step on the low parts.
+template <int CB, bool kRot>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a) {
   constexpr bool kPacked = CB != 16;
+  static_assert(!kRot || kPacked, "rotation needs a packed layout");
   constexpr bool kTypeB = CB == 2;  // pairing of the content groups
   constexpr PageGeom G = page_geom(CB);
   extern __shared__ __align__(128) uint8_t smem[];
   __half* qs = reinterpret_cast<__half*>(smem + kOffQ);
+  __half* qs_lo = reinterpret_cast<__half*>(smem + kOffTeam + kTeams * team_bytes(CB));
   float* qsum = reinterpret_cast<float*>(smem + kOffQsum);
   int* scan = reinterpret_cast<int*>(smem + kOffScan);
 
@@ -174,18 +183,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       uint4 v[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) v[c] = src[c];
-      float acc = 0.f;
+      float f[64];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int p = c * 8 + e;
-          const float f = (e & 1) ? bf16hi_to_f32(w[e >> 1]) : bf16lo_to_f32(w[e >> 1]);
-          const __half hv = __float2half_rn(f);
-          acc += __half2float(hv);
-          qs[h * kQStride + g * 64 + logical_of_phys(p, tb)] = hv;
+        for (int e = 0; e < 8; ++e)
+          f[c * 8 + e] = (e & 1) ? bf16hi_to_f32(w[e >> 1]) : bf16lo_to_f32(w[e >> 1]);
+      }
+      if (kRot && g < 8) {
+        // R q for this content group: the same orthonormal Hadamard rotation
+        // as the stored latent (the order of operations does not matter here)
+#pragma unroll
+        for (int hh = 1; hh < 64; hh <<= 1) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (i & hh) continue;
+            const float x = f[i], y = f[i + hh];
+            f[i] = x + y;
+            f[i + hh] = x - y;
+          }
         }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) f[i] *= 0.125f;
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int p = 0; p < 64; ++p) {
+        const __half hv = __float2half_rn(f[p]);
+        const __half lv = __float2half_rn(f[p] - __half2float(hv));
+        acc += __half2float(hv);
+        if (kRot) acc += __half2float(lv);
+        qs[h * kQStride + g * 64 + logical_of_phys(p, tb)] = hv;
+        if (kRot) qs_lo[h * kQStride + g * 64 + logical_of_phys(p, tb)] = lv;
       }
       qsum[g * kHC + h] = acc;
     }
@@ -295,6 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
               uint32_t af[4];
               ldmatrix_x4(af, qs + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
               mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
+              if (kRot && g < 8) {
+                ldmatrix_x4(af, qs_lo + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
+                mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
+              }
             }
             const float centre = (g < 8 && CB == 2) ? float(kCentre2) : float(kCentre4);
             const float2 sm0 = __half22float2(*reinterpret_cast<const __half2*>(&mt0));
@@ -382,6 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
           uint32_t af[4];
           ldmatrix_x4(af, qs + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
           mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
+          if (kRot && g < 8) {
+            ldmatrix_x4(af, qs_lo + (lane & 15) * kQStride + g * 64 + s * 16 + (lane >> 4) * 8);
+            mma_16816(D, af, bq[2 * s], bq[2 * s + 1]);
+          }
         }
         S[0] += D[0];
         S[1] += D[1];
@@ -572,6 +610,7 @@ struct CombineArgs {
   float* out;
   float* lse;
   int B, H, total_splits;
+  int rotate;  // the splits hold R o for each content group: apply R (= R^T) back
 };
 
 constexpr int kCombineWarps = 2;  // 128-channel quarters per block
@@ -637,6 +676,28 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     acc.z = fmaf(w, v.z, acc.z);
     acc.w = fmaf(w, v.w, acc.w);
   }
+  if (a.rotate) {
+    // Sylvester H64 / 8 over the group of 16 lanes (4 channels each) this
+    // lane belongs to: stages 1 and 2 inside the lane, 4..32 across lanes
+    float x[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int hh = 1; hh < 4; hh <<= 1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (!(i & hh)) {
+          const float u = x[i], v = x[i + hh];
+          x[i] = u + v;
+          x[i + hh] = u - v;
+        }
+#pragma unroll
+    for (int lb = 1; lb < 16; lb <<= 1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __shfl_xor_sync(0xffffffffu, x[i], lb);
+        x[i] = (lane & lb) ? p - x[i] : x[i] + p;
+      }
+    acc = make_float4(x[0] * 0.125f, x[1] * 0.125f, x[2] * 0.125f, x[3] * 0.125f);
+  }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   *reinterpret_cast<float4*>(a.out + ((long long)b * a.H + h) * kLatent + c) =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -668,8 +729,9 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
 // layouts, the hybrid mma.sync + tcgen05 kernel ("hy", decode_hy.cu) or the
 // all-tcgen05 kernel ("tc", decode_tc.cu).
 enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp };
-static SplitKernel split_kernel(int cbits, int n_q = 1) {
-  if (cbits == 16 || n_q > 1) return SplitKernel::kMma;  // the only one with query blocks
+static SplitKernel split_kernel(int cbits, int n_q = 1, int rotate = 0) {
+  // the only one with query blocks and with rotated queries
+  if (cbits == 16 || n_q > 1 || rotate) return SplitKernel::kMma;
   const char* v = getenv("MLA_LOWBIT_DECODE");
   if (v && v[0] == 'h') return SplitKernel::kHybrid;
   if (v && v[0] == 't') return SplitKernel::kTc;
@@ -683,39 +745,33 @@ bool decode_fuses_append(int cbits) {
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream) {
-  const SplitKernel sk = split_kernel(cbits, a.n_q);
+  const SplitKernel sk = split_kernel(cbits, a.n_q, a.rotate);
   if (sk != SplitKernel::kMma) {
     cudaError_t et = sk == SplitKernel::kTc     ? launch_decode_tc(cbits, a, stream)
                      : sk == SplitKernel::kHybrid ? launch_decode_hy(cbits, a, stream)
                                                   : launch_decode_gw(cbits, a, stream);
     if (et != cudaSuccess) return et;
-    CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
+    CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits, 0};
     return launch_combine(ca, stream);
   }
-  static bool configured[3] = {false, false, false};
-  const int k = cbits == 4 ? 0 : cbits == 2 ? 1 : 2;
+  const bool rot = a.rotate && cbits != 16;
+  void (*kern)(DecodeArgs) = cbits == 4   ? (rot ? decode_split_kernel<4, true> : decode_split_kernel<4, false>)
+                             : cbits == 2 ? (rot ? decode_split_kernel<2, true> : decode_split_kernel<2, false>)
+                                          : decode_split_kernel<16, false>;
+  const int smem = smem_bytes(cbits, rot);
+  static bool configured[5] = {false, false, false, false, false};
+  const int k = cbits == 16 ? 4 : (cbits == 4 ? 0 : 2) + (rot ? 1 : 0);
   cudaError_t e = cudaSuccess;
   if (!configured[k]) {
-    switch (cbits) {
-      case 4: e = cudaFuncSetAttribute(decode_split_kernel<4>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(4)); break;
-      case 2: e = cudaFuncSetAttribute(decode_split_kernel<2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2)); break;
-      default: e = cudaFuncSetAttribute(decode_split_kernel<16>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(16));
-    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[k] = true;
   }
   dim3 grid(a.total_splits, a.H / kHC), block(kThreads);
-  switch (cbits) {
-    case 4: decode_split_kernel<4><<<grid, block, smem_bytes(4), stream>>>(a); break;
-    case 2: decode_split_kernel<2><<<grid, block, smem_bytes(2), stream>>>(a); break;
-    default: decode_split_kernel<16><<<grid, block, smem_bytes(16), stream>>>(a);
-  }
+  kern<<<grid, block, smem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits};
+  CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits, rot ? 1 : 0};
   return launch_combine(ca, stream);
 }
 

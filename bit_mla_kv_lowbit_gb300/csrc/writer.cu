@@ -42,8 +42,9 @@ __global__ void __launch_bounds__(kGroups * 32) writer_kernel(WriterArgs a) {
   uint8_t* base = a.pool + page * G.page_bytes;
 
   // Lane holds channels (2*lane, 2*lane+1) of this group.
-  const uint32_t v = g < 8 ? a.ckv[(long long)i * (kLatent / 2) + g * 32 + lane]
-                           : a.krope[(long long)i * (kRope / 2) + lane];
+  uint32_t v = g < 8 ? a.ckv[(long long)i * (kLatent / 2) + g * 32 + lane]
+                     : a.krope[(long long)i * (kRope / 2) + lane];
+  if (a.rotate && g < 8) v = rotate_group_bf16(v, lane);  // whole warp: g is warp-uniform
 
   if constexpr (CB == 16) {
     reinterpret_cast<uint32_t*>(base + row * G.content_row)[g * 32 + lane] = v;

@@ -8,9 +8,35 @@
 // compiler contraction), codes are rounded half to even, clamped and packed.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace mlalb {
+
+// Online rotation of one 64-channel content group held by a warp as bf16 pairs
+// (lane l: channels 2l, 2l+1): R x with R = H_64 / 8, float32 butterflies in
+// the layout's order (stage h pairs element i, bit h clear, with i + h into
+// (a + b, a - b); h = 1 inside the lane, h >= 2 across lanes l ^ h/2), then
+// x 1/8 (exact), rounded to bf16 (nearest even).  All 32 lanes must call it.
+__device__ __forceinline__ uint32_t rotate_group_bf16(uint32_t v, int lane) {
+  const float a = bf16lo_to_f32(v), b = bf16hi_to_f32(v);
+  float x0 = __fadd_rn(a, b), x1 = __fsub_rn(a, b);
+#pragma unroll
+  for (int hl = 1; hl < 32; hl <<= 1) {
+    const float p0 = __shfl_xor_sync(0xffffffffu, x0, hl);
+    const float p1 = __shfl_xor_sync(0xffffffffu, x1, hl);
+    if (lane & hl) {  // this element is the second of its pair: partner - own
+      x0 = __fsub_rn(p0, x0);
+      x1 = __fsub_rn(p1, x1);
+    } else {
+      x0 = __fadd_rn(x0, p0);
+      x1 = __fadd_rn(x1, p1);
+    }
+  }
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 * 0.125f, x1 * 0.125f);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
 // Quantise and store group g (0..7 content, 8 RoPE) of the token in row `row`
 // of the packed page at `page_base`.  All 32 lanes of the warp must call it.

@@ -56,6 +56,17 @@ typedef struct mla_lowbit_layout {
   int page_tokens;  /* 64: tokens per page */
   int latent;       /* 512: content latent width (kv_lora_rank) */
   int rope;         /* 64: RoPE key width (qk_rope_head_dim) */
+  int rotate;       /* 0, or 1 (packed layouts): online Hadamard rotation of the content
+                       latent -- the writer replaces each 64-channel content group x by
+                       R x, R = H_64 / 8 (orthonormal Sylvester-Hadamard; float32
+                       butterfly stages h = 1, 2, .., 32, element i (bit h clear) and
+                       i + h becoming (a + b, a - b), then x 1/8), rounded to bf16, for the
+                       packed codes and the bf16 copies alike; decode rotates the
+                       queries' content channels by R and rotates outputs back, so the
+                       result is attention over R^T of the stored keys.  RoPE keys are
+                       not rotated.  (QuantMLA, Table 1: QuaRot as an MLA-adapted
+                       baseline; the pages' own transforms are fused offline -- this is
+                       the un-fused variant.) */
 } mla_lowbit_layout;
 
 enum {

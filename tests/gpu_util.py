@@ -33,7 +33,7 @@ def to_dev(a, dtype, dev="cuda"):
 class GpuRun:
     """One workload on the GPU: prefill, then ``steps`` writer + decode steps."""
 
-    def __init__(self, w: syn.Workload, dev: str = "cuda"):
+    def __init__(self, w: syn.Workload, dev: str = "cuda", rotate: bool = False):
         import torch
         import bit_mla_kv_lowbit_gb300 as pkg
         self.torch = torch
@@ -41,7 +41,9 @@ class GpuRun:
         self.dev = dev
         self.lens = syn.sequence_lengths(w)
         self.table, self.npages = syn.make_paging(w)
-        self.cache = pkg.PagedCache(w.content_bits, w.rope_bits, self.table, self.npages, dev)
+        self.rotate = rotate
+        self.cache = pkg.PagedCache(w.content_bits, w.rope_bits, self.table, self.npages, dev,
+                                    rotate=rotate)
         self.scales = syn.channel_scales(w)
         self.tokens = {}
         self.step = -1
@@ -115,7 +117,7 @@ class GpuRun:
 def oracle_model(run: GpuRun, b: int, s: int):
     """Oracle cache model holding sequence b after step s (its own writer)."""
     w = run.w
-    lay = oracle.Layout(w.content_bits, w.rope_bits)
+    lay = oracle.Layout(w.content_bits, w.rope_bits, rotate=run.rotate)
     model = oracle.PagedCacheModel(lay, run.npages, run.table)
     L = int(run.lens[b]) + s
     ckv, kr = run.seq_tokens(b)

@@ -41,7 +41,7 @@ def test_sizes_agree_with_oracle_closed_form():
 
 @pytest.mark.parametrize("fields", [
     dict(content_bits=3), dict(rope_bits=2), dict(group=32), dict(sink=0), dict(local=64),
-    dict(page_tokens=128), dict(latent=256), dict(rope=32),
+    dict(page_tokens=128), dict(latent=256), dict(rope=32), dict(rotate=2), dict(rotate=-1),
 ])
 def test_invalid_layouts_rejected(fields):
     lay = pkg.layout(4, 4)
@@ -50,6 +50,14 @@ def test_invalid_layouts_rejected(fields):
     assert pkg.page_bytes(lay) == 0
     with pytest.raises(pkg.LibraryError):
         pkg.decode_plan(lay, 16, [100], num_sms=152)
+
+
+def test_rotation_only_on_packed_layouts():
+    # the online rotation re-encodes the content latent before quantisation:
+    # accepted for the packed layouts, refused for bf16 pages
+    for cb in (4, 2):
+        assert pkg.page_bytes(pkg.layout(cb, 4, rotate=True)) == pkg.page_bytes(pkg.layout(cb, 4))
+    assert pkg.page_bytes(pkg.layout(16, 16, rotate=True)) == 0
 
 
 def test_strerror_and_version():

@@ -29,7 +29,8 @@ def _check_run_step(run, s, seqs=None, lse=None, fused=False):
         got_pages = run.cache.pool[run.torch.from_numpy(pages.astype(np.int64)).to(run.dev)]
         assert np.array_equal(got_pages.cpu().numpy(), model.pool[pages]), f"writer bytes, seq {b}"
         q = syn.queries(run.w, b)[s]
-        ref, ref_lse = oracle.mla_decode_fp64(q, model.effective_keys(b, L), run.w.softmax_scale)
+        ref, ref_lse = oracle.mla_decode_fp64(q, model.effective_keys(b, L), run.w.softmax_scale,
+                                              rotate=run.rotate)
         check_attention(out[b], ref, f"{run.w.name} seq {b} (L={L}) step {s}")
         if lse_got is not None:
             assert np.allclose(lse_got[b], ref_lse, rtol=0, atol=1e-4), f"lse seq {b}"
