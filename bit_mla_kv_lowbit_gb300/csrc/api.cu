@@ -173,9 +173,8 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, i
   if (st != MLA_LOWBIT_OK) return st;
   if (workspace_bytes < need) return MLA_LOWBIT_EWORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the fused append reads the new token's unrotated input: not with rotation
-  const bool fused = append && n_q == 1 && !layout->rotate &&
-                     decode_fuses_append(layout->content_bits);
+  const bool fused = append && n_q == 1 &&
+                     decode_fuses_append(layout->content_bits, layout->rotate);
   if (append && !fused) {
     WriterArgs w;
     w.ckv = static_cast<const uint32_t*>(ckv_new);

@@ -176,7 +176,7 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
                           cudaStream_t stream);
 // True when launch_decode can append each sequence's new token itself (the
 // DecodeArgs new_* fields): the default split kernel on a packed layout.
-bool decode_fuses_append(int cbits);
+bool decode_fuses_append(int cbits, int rotate);
 cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_hy(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_gw(int cbits, const DecodeArgs& a, cudaStream_t stream);

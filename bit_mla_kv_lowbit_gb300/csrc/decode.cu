@@ -58,9 +58,10 @@ constexpr int kTOffStage = kTOffMax + kTeamWarps * kHC * 4;
 __host__ __device__ constexpr int team_bytes(int cbits) {
   return kTOffStage + (cbits == 16 ? 0 : page_geom(cbits).page_bytes);
 }
-// a rotated q keeps its low fp16 parts after the two teams
+// a rotated q keeps its low fp16 parts after the two teams, then the rotated
+// content latent of the appended token
 __host__ __device__ constexpr int smem_bytes(int cbits, bool rot = false) {
-  return kOffTeam + kTeams * team_bytes(cbits) + (rot ? kQBytes : 0);
+  return kOffTeam + kTeams * team_bytes(cbits) + (rot ? kQBytes + kLatent * 2 : 0);
 }
 static_assert(smem_bytes(4, true) <= 227 * 1024, "shared memory budget");
 
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   extern __shared__ __align__(128) uint8_t smem[];
   __half* qs = reinterpret_cast<__half*>(smem + kOffQ);
   __half* qs_lo = reinterpret_cast<__half*>(smem + kOffTeam + kTeams * team_bytes(CB));
+  uint32_t* new_rot = reinterpret_cast<uint32_t*>(smem + kOffTeam + kTeams * team_bytes(CB) + kQBytes);
   float* qsum = reinterpret_cast<float*>(smem + kOffQsum);
   int* scan = reinterpret_cast<int*>(smem + kOffScan);
 
@@ -240,13 +242,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   // fused append: the sequence's new token (position L - 1) is packed into its
   // page and copied to the bf16 buffers by head chunk 0's bf16 split, one warp
   // per group.  No split reads those bytes in this call: the token is inside
-  // the recent window, and every bf16 split reads it from the input below.
+  // the recent window, and every bf16 split reads it from the input below (a
+  // rotated cache: the split's rotated copy of it in shared memory).
   if constexpr (kPacked) {
+    if (kRot && sw.has_last && a.new_ckv && L >= 1) {
+      if ((tid >> 5) < 8) {
+        const int gwp = tid >> 5;
+        new_rot[gwp * 32 + lane] =
+            rotate_group_bf16(a.new_ckv[(long long)b * (kLatent / 2) + gwp * 32 + lane], lane);
+      }
+      __syncthreads();  // CTA-uniform condition
+    }
     if (sw.has_last && a.new_ckv && hc == 0 && L >= 1 && (tid >> 5) < kGroups) {
       const int gwp = tid >> 5, pos = L - 1;
       const long long page = a.block_table[(long long)b * a.max_pages + pos / kPageTokens];
       if (page >= 0 && page < a.num_pages) {
-        const uint32_t v = gwp < 8 ? a.new_ckv[(long long)b * (kLatent / 2) + gwp * 32 + lane]
+        const uint32_t v = gwp < 8 ? (kRot ? new_rot[gwp * 32 + lane]
+                                           : a.new_ckv[(long long)b * (kLatent / 2) + gwp * 32 + lane])
                                    : a.new_kr[(long long)b * (kRope / 2) + lane];
         if (pos < kSink) a.sink_w[((long long)b * kSink + pos) * (kDim / 2) + gwp * 32 + lane] = v;
         a.recent_w[((long long)b * kLocal + pos % kLocal) * (kDim / 2) + gwp * 32 + lane] = v;
@@ -372,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
         if (i < sw.n_tok) {
           const int pos = bf16_pos(sw, i);
           if (a.new_ckv && pos == L - 1) {
-            rowptr = reinterpret_cast<const uint16_t*>(a.new_ckv) + (long long)b * kLatent;
+            rowptr = kRot ? reinterpret_cast<const uint16_t*>(new_rot)
+                          : reinterpret_cast<const uint16_t*>(a.new_ckv) + (long long)b * kLatent;
             rope_ptr = reinterpret_cast<const uint16_t*>(a.new_kr) + (long long)b * kRope;
           } else {
             rowptr = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
@@ -739,8 +752,8 @@ static SplitKernel split_kernel(int cbits, int n_q = 1, int rotate = 0) {
   return SplitKernel::kMma;
 }
 
-bool decode_fuses_append(int cbits) {
-  return cbits != 16 && split_kernel(cbits) == SplitKernel::kMma;
+bool decode_fuses_append(int cbits, int rotate) {
+  return cbits != 16 && split_kernel(cbits, 1, rotate) == SplitKernel::kMma;
 }
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,

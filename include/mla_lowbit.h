@@ -196,8 +196,9 @@ int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
  * identical to that pair of calls.  For packed layouts on the default split
  * kernel both happen in the decode launch (the new token is inside the recent
  * window, so no packed split reads the bytes being written, and the bf16
- * split reads the new values from ckv_new/krope_new); otherwise the writer
- * kernel runs first on `stream`.
+ * split reads the new values from ckv_new/krope_new, rotating the content
+ * latent itself on a rotated layout); otherwise the writer kernel runs first
+ * on `stream`.
  *
  *   ckv_new    [num_seqs][512] bf16, krope_new [num_seqs][64] bf16 (16-byte aligned)
  *   seq_lens   device, every entry >= 1 (seq_lens_host the same values)

@@ -34,8 +34,9 @@ def test_rotated_head_counts(heads):
 
 
 def test_rotated_write_decode_entry():
-    # mla_lowbit_write_decode on a rotated cache: the append runs as the
-    # writer (the fused append reads the unrotated input), same results
+    # mla_lowbit_write_decode on a rotated cache: the append is fused into
+    # the decode launch, which rotates the new token itself; the bytes it
+    # writes and the attention must match the oracle's writer + decode
     w = syn.custom("rot_wd", [1, 5, 132, 133, 197, 1000, 4099], heads=16, content_bits=4,
                    steps=3, seed=73)
     run = GpuRun(w, rotate=True)
