@@ -112,7 +112,8 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
     if (seq_lens_host[b] < 0) return MLA_LOWBIT_EINVAL;
     work += units_of(seq_lens_host[b], packed);
   }
-  const long long head_chunks = heads / 16;
+  const long long head_chunks =
+      decode_ctas_per_split(layout->content_bits, heads, layout->rotate);
   const long long slots = (long long)num_sms * kCtasPerSm;
   // equal chunks of work units (pages, then the protected tokens' bf16 tiles)
   // so that all splits of all head chunks fit one wave when they can
@@ -120,10 +121,20 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   if (chunk < 1) chunk = 1;
   // a split accumulates at most kMaxChunkPages * 64 tokens in fp32 tensor-core
   // accumulators (whose adds are not round-to-nearest); longer sequences get
-  // more splits, merged in fp32 by the combine kernel
-  if (chunk > kMaxChunkPages) chunk = kMaxChunkPages;
+  // more splits, merged in fp32 by the combine kernel.  With several waves,
+  // the work is spread evenly over all of them rather than leaving a sliver
+  // for the last one; then the chunk grows until the per-sequence rounding
+  // of the splits fits those waves.
+  const long long waves = (chunk + kMaxChunkPages - 1) / kMaxChunkPages;
+  chunk = (work * head_chunks + slots * waves - 1) / (slots * waves);
+  if (chunk < 1) chunk = 1;
   long long total = 0;
-  for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
+  for (;;) {
+    total = 0;
+    for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
+    if (total * head_chunks <= slots * waves || chunk >= kMaxChunkPages) break;
+    ++chunk;
+  }
   if (total > INT32_MAX / 2) return MLA_LOWBIT_ESIZE;
   *total_splits = (int)total;
   *chunk_pages = (int)chunk;
@@ -174,7 +185,7 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, i
   if (workspace_bytes < need) return MLA_LOWBIT_EWORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool fused = append && n_q == 1 &&
-                     decode_fuses_append(layout->content_bits, layout->rotate);
+                     decode_fuses_append(layout->content_bits, layout->rotate, heads);
   if (append && !fused) {
     WriterArgs w;
     w.ckv = static_cast<const uint32_t*>(ckv_new);

@@ -737,31 +737,42 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, combine_kernel, ca);
 }
 
-// Kernel for a layout: the mma.sync kernel above (the fastest measured on
-// GB300 for 16-head chunks) unless MLA_LOWBIT_DECODE selects, for packed
-// layouts, the hybrid mma.sync + tcgen05 kernel ("hy", decode_hy.cu) or the
-// all-tcgen05 kernel ("tc", decode_tc.cu).
-enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp };
-static SplitKernel split_kernel(int cbits, int n_q = 1, int rotate = 0) {
+// Kernel for a layout and a row count (n_q * heads): packed caches with
+// exactly 128 rows and no rotation take the 2-CTA tcgen05 kernel
+// (decode_wide.cu); everything else the mma.sync kernel above (the fastest
+// measured on GB300 for 16-head chunks).  MLA_LOWBIT_DECODE overrides the
+// choice: "m" always the mma.sync kernel; for packed single-query
+// unrotated decodes "h" the hybrid mma.sync + tcgen05 kernel (decode_hy.cu),
+// "t" the all-tcgen05 16-head kernel (decode_tc.cu), "g" the group-per-warp
+// kernel (decode_gw.cu).
+enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp, kWide };
+static SplitKernel split_kernel(int cbits, int n_q, int rotate, int rows) {
+  const char* v = getenv("MLA_LOWBIT_DECODE");
+  const char k = v ? v[0] : 0;
+  if (k == 0 && cbits != 16 && !rotate && rows == 128) return SplitKernel::kWide;
   // the only one with query blocks and with rotated queries
   if (cbits == 16 || n_q > 1 || rotate) return SplitKernel::kMma;
-  const char* v = getenv("MLA_LOWBIT_DECODE");
-  if (v && v[0] == 'h') return SplitKernel::kHybrid;
-  if (v && v[0] == 't') return SplitKernel::kTc;
-  if (v && v[0] == 'g') return SplitKernel::kGroupWarp;
+  if (k == 'h') return SplitKernel::kHybrid;
+  if (k == 't') return SplitKernel::kTc;
+  if (k == 'g') return SplitKernel::kGroupWarp;
   return SplitKernel::kMma;
 }
 
-bool decode_fuses_append(int cbits, int rotate) {
-  return cbits != 16 && split_kernel(cbits, 1, rotate) == SplitKernel::kMma;
+int decode_ctas_per_split(int cbits, int rows, int rotate) {
+  return split_kernel(cbits, 1, rotate, rows) == SplitKernel::kWide ? 2 : rows / kHC;
+}
+
+bool decode_fuses_append(int cbits, int rotate, int rows) {
+  return cbits != 16 && split_kernel(cbits, 1, rotate, rows) == SplitKernel::kMma;
 }
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream) {
-  const SplitKernel sk = split_kernel(cbits, a.n_q, a.rotate);
+  const SplitKernel sk = split_kernel(cbits, a.n_q, a.rotate, a.H);
   if (sk != SplitKernel::kMma) {
-    cudaError_t et = sk == SplitKernel::kTc     ? launch_decode_tc(cbits, a, stream)
+    cudaError_t et = sk == SplitKernel::kTc       ? launch_decode_tc(cbits, a, stream)
                      : sk == SplitKernel::kHybrid ? launch_decode_hy(cbits, a, stream)
+                     : sk == SplitKernel::kWide   ? launch_decode_wide(cbits, a, stream)
                                                   : launch_decode_gw(cbits, a, stream);
     if (et != cudaSuccess) return et;
     CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits, 0};
