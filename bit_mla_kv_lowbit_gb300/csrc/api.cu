@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/mla_lowbit.h: argument checks,
 // split planning and kernel launches.  No device memory is allocated here.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -125,15 +126,23 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   // the work is spread evenly over all of them rather than leaving a sliver
   // for the last one; then the chunk grows until the per-sequence rounding
   // of the splits fits those waves.
-  const long long waves = (chunk + kMaxChunkPages - 1) / kMaxChunkPages;
-  chunk = (work * head_chunks + slots * waves - 1) / (slots * waves);
-  if (chunk < 1) chunk = 1;
+  // If no chunk up to the cap fits that many waves, the next wave count is
+  // tried, starting from the fewest waves that the capped chunk allows.
   long long total = 0;
-  for (;;) {
-    total = 0;
-    for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
-    if (total * head_chunks <= slots * waves || chunk >= kMaxChunkPages) break;
-    ++chunk;
+  for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)kMaxChunkPages);
+  long long waves = (chunk + kMaxChunkPages - 1) / kMaxChunkPages;
+  waves = std::max(waves, (total * head_chunks + slots - 1) / slots);
+  for (;; ++waves) {
+    chunk = (work * head_chunks + slots * waves - 1) / (slots * waves);
+    if (chunk < 1) chunk = 1;
+    if (chunk > kMaxChunkPages) chunk = kMaxChunkPages;
+    for (;;) {
+      total = 0;
+      for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
+      if (total * head_chunks <= slots * waves || chunk >= kMaxChunkPages) break;
+      ++chunk;
+    }
+    if (total * head_chunks <= slots * waves || chunk == 1) break;
   }
   if (total > INT32_MAX / 2) return MLA_LOWBIT_ESIZE;
   *total_splits = (int)total;
