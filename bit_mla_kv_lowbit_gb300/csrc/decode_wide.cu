@@ -57,7 +57,8 @@ constexpr int kXStride = 36;                                 // floats per excha
 constexpr int kOffX = kOffA + kNB * kMaxOwn * kPlane;        // [2 halves][128 rows][kXStride] fp32
 constexpr int kOffMeta = kOffX + 2 * kRows * kXStride * 4;   // [kNB][5][64] fp32 (s, m')
 constexpr int kOffValid = kOffMeta + kNB * kMaxOwn * 64 * 8; // [kNB][2] token masks
-constexpr int kOffMax = kOffValid + kNB * 2 * 4;             // [2][2][128] fp32
+constexpr int kOffSmax = kOffValid + kNB * 2 * 4;            // [kNB][4] largest PV scale per unpack warp
+constexpr int kOffMax = kOffSmax + kNB * 4 * 4;              // [2][2][128] fp32
 constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
 constexpr int kOffPages = kOffScan + 32 * 4;                 // [64] page ids of the split
 constexpr int kOffBar = kOffPages + 64 * 4;
@@ -229,6 +230,16 @@ __device__ __forceinline__ bool pair_any(bool pred, int qd) {
 // Wait results made warp-uniform before any .sync.aligned tensor-memory access.
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// x = hi + lo with hi = x cut to 11 significant bits (exact in fp16 over its
+// normal range) and lo = the exact float32 remainder rounded to fp16: x to
+// about 2^-21 relative, in fewer instructions than rounding hi.
+__device__ __forceinline__ void split_trunc(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const float ha = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
+  const float hb = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
+  hi = pack_half2(ha, hb);
+  lo = pack_half2(a - ha, b - hb);
+}
+
 // Global group of local QK group j of rank r.
 __device__ __forceinline__ int group_of(int r, int j) { return j < 4 ? 4 * r + j : 8; }
 
@@ -245,6 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   float2* sMeta = reinterpret_cast<float2*>(smem + kOffMeta);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + kOffValid);
   float* sMax = reinterpret_cast<float*>(smem + kOffMax);
+  float* sSmax = reinterpret_cast<float*>(smem + kOffSmax);
   int* scan = reinterpret_cast<int*>(smem + kOffScan);
   int* s_pages = reinterpret_cast<int*>(smem + kOffPages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -430,6 +442,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const uint32_t mk = __ballot_sync(0xffffffffu, okt_cur);
         if (pp == 0 && lane == 0) sMask[buf * 2 + (t >> 5)] = mk;
+        // largest scale of the PV groups in this tile (bounds P * s in fp16)
+        float smx = fmaxf(meta[(2 * pp) * 64 + t].x, meta[(2 * pp + 1) * 64 + t].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, o));
+        if (lane == 0) sSmax[buf * 4 + warp] = smx;
       } else {
         // protected tokens: bf16 values in place of codes, scale 1, min 0
         const int idx = bf_first + (i - n_pk) * 64 + t;
@@ -479,6 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const uint32_t mk = __ballot_sync(0xffffffffu, okt);
         if (pp == 0 && lane == 0) sMask[buf * 2 + (t >> 5)] = mk;
+        if (lane == 0) sSmax[buf * 4 + warp] = 1.f;
       }
       tc::fence_async_smem();
       tc::bar_arrive(bar(kBarAFull + buf));
@@ -584,7 +602,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       sMax[((i & 1) * 2 + th) * kRows + h] = mx;
       if (pair_any(!ok, qd)) break;  // both warps of the rows leave at the same tile
       const float tmax = fmaxf(sMax[((i & 1) * 2) * kRows + h], sMax[((i & 1) * 2 + 1) * kRows + h]);
-      const bool need = m_run != -INFINITY && tmax > m_run + kLazy;
+      // lazy max: moved only when the tile max exceeds it by kLazy, or by less
+      // when the tile's largest scale s would take P * s <= 2^kLazy * s past
+      // the fp16 range
+      const float smax = fmaxf(fmaxf(sSmax[buf * 4], sSmax[buf * 4 + 1]),
+                               fmaxf(sSmax[buf * 4 + 2], sSmax[buf * 4 + 3]));
+      const float lim = smax > 0.f ? fmaxf(0.f, fminf(kLazy, log2f(32768.f / smax))) : kLazy;
+      const bool need = m_run != -INFINITY && tmax > m_run + lim;
       const float m_new = (m_run == -INFINITY || need) ? tmax : m_run;
       if (__any_sync(0xffffffffu, need)) {
         // rescale what PV has accumulated so far (previous tile's PV done)
@@ -631,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float4 mv = m4[t2];  // (s, m') of tokens 2 t2, 2 t2 + 1
           const float p0 = S[2 * t2], p1 = S[2 * t2 + 1];
           am = fmaf(p0, mv.y, fmaf(p1, mv.w, am));
-          split_hi_lo(p0 * mv.x, p1 * mv.z, hi[t2], lo[t2]);
+          split_trunc(p0 * mv.x, p1 * mv.z, hi[t2], lo[t2]);
         }
         accm[j] += am;
         tmem_st16_nowait(tl + kColPs + 64 * pslot + 16 * th, hi);

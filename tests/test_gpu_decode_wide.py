@@ -94,3 +94,40 @@ def test_wide_multi_query_blocks(cb, heads, n):
         for i in range(n):
             check_attention(out[b, i], ref[i], f"seq {b} (L={L}) query {i}")
             assert np.allclose(lse[b, i], ref_lse[i], rtol=0, atol=1e-4), f"lse seq {b} query {i}"
+
+
+def test_wide_large_scales_under_the_lazy_max():
+    # Content groups spanning +-3000 (fp16 scales near 400) and logits that
+    # climb slowly along the sequence, so the running max trails the tile max
+    # by up to the lazy threshold: P * s would pass the fp16 range unless the
+    # tile's largest scale lowers the threshold.  Outputs are O(1e3), so the
+    # bar is relative: rel-L2 <= 1e-3 and max-abs <= 1e-5 of the largest value.
+    import torch
+    import bit_mla_kv_lowbit_gb300 as pkg
+    rng = np.random.default_rng(91)
+    L, H = 2000, 128
+    ckv = rng.uniform(-3000.0, 3000.0, (L, 512))
+    u = np.where(rng.random(64) < 0.5, -0.125, 0.125)
+    ramp = 0.5 + 3.0 * np.arange(L) / L
+    kr = ramp[:, None] * u[None, :]
+    q = np.zeros((H, 576))
+    q[:, 512:] = 130.0 * u[None, :] * (1.0 + 0.01 * np.arange(H))[:, None]
+    to_bits = lambda x: syn.bf16_bits_from_f32(np.asarray(x, dtype=np.float32))
+    ckv_b, kr_b, q_b = to_bits(ckv), to_bits(kr), to_bits(q)
+    table = np.arange(32, dtype=np.int32)[None, :]
+    cache = pkg.PagedCache(4, 4, table, 32, "cuda")
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    cache.write(to_dev(ckv_b, torch.bfloat16), to_dev(kr_b, torch.bfloat16),
+                torch.arange(L, dtype=torch.int32, device="cuda"),
+                seq_idx=torch.zeros(L, dtype=torch.int32, device="cuda"), seq_lens_after=lens)
+    scale = 1.0 / np.sqrt(192.0)
+    out = cache.decode(to_dev(q_b[None], torch.bfloat16), lens, [L], scale)
+    torch.cuda.synchronize()
+    assert cache.error() == 0
+    got = out.cpu().numpy()[0].astype(np.float64)
+    model = oracle.PagedCacheModel(oracle.Layout(4, 4), 32, table)
+    model.write(np.zeros(L, np.int64), np.arange(L), ckv_b, kr_b, np.array([L]))
+    ref, _ = oracle.mla_decode_fp64(q_b, model.effective_keys(0, L), scale)
+    assert np.all(np.isfinite(got))
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= 1e-3 and np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max(), (rel, np.abs(got - ref).max())
