@@ -154,14 +154,21 @@ def traffic_record(kernel_key: str):
         return None
     if not rec:
         return None
-    import hashlib
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(os.path.join(ROOT, "bit_mla_kv_lowbit_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "bit_mla_kv_lowbit_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if rec.get("csrc_sha256") != h.hexdigest():
+    if rec.get("sources_sha256") != sources_sha256(rec.get("sources", [])):
         return None
     return rec
+
+
+def sources_sha256(files):
+    """Hash of the files (repo-relative) that define a captured kernel and its launch."""
+    import hashlib
+    h = hashlib.sha256()
+    if not files:
+        return None
+    for name in files:
+        with open(os.path.join(ROOT, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # ---------------------------------------------------------------- the GPU arm
