@@ -24,13 +24,14 @@
 // * O (128 x 256 fp32) lives in tensor memory for the whole split and is
 //   rescaled only when a row's running max grows by more than kLazy.
 //
-// Warp roles (416 threads, one CTA per SM):
+// Warp roles (672 threads, one CTA per SM):
 //   warps 0-3   unpack: packed bytes -> fp16 code planes and metadata; the
 //               next tile's bytes are loaded into registers while a plane
 //               buffer is still in use;
-//   warps 4-11  softmax: TMEM lane quadrant w & 3 (32 rows), token half
-//               (w - 4) >> 2; fold, exchange, softmax, P*s operands;
-//   warp 12     MMA issue (one lane) and the TMEM allocation.
+//   warps 4-19  softmax: TMEM lane quadrant w & 3 (32 rows), token quarter
+//               (w - 4) >> 2 (16 tokens); fold, exchange, softmax, P*s
+//               operands;
+//   warp 20     MMA issue (one lane) and the TMEM allocation.
 // Every wait is bounded; on a time-out the CTA records MLA_LOWBIT_DEV_PIPELINE,
 // the softmax warps leave the tile loop together (barrier reduction), the
 // partial is written empty, and tensor memory is still freed.
@@ -41,9 +42,10 @@ namespace mlalb {
 namespace wide {
 
 constexpr int kRows = 128;
-constexpr int kThreads = 416;
-constexpr int kSoftThreads = 256;
-constexpr int kIssuerWarp = 12;
+constexpr int kThreads = 672;
+constexpr int kSoftThreads = 512;
+constexpr int kTW = 16;                 // tokens of a tile per softmax warp
+constexpr int kIssuerWarp = 20;
 constexpr int kNB = 2;                  // code-plane ring depth (tiles)
 constexpr int kMaxOwn = 5;              // QK groups of a CTA
 constexpr int kPlane = 64 * 128;        // 64 tokens x 64 fp16 (128-byte rows)
@@ -53,13 +55,13 @@ constexpr float kLazy = 8.0f;           // log2 units
 // shared memory (bytes, from a 1 KB aligned base)
 constexpr int kOffQ = 0;                                     // [5] q blocks
 constexpr int kOffA = kOffQ + kMaxOwn * kQBlock;             // [kNB][5] planes
-constexpr int kXStride = 36;                                 // floats per exchange row (padded)
-constexpr int kOffX = kOffA + kNB * kMaxOwn * kPlane;        // [2 halves][128 rows][kXStride] fp32
-constexpr int kOffMeta = kOffX + 2 * kRows * kXStride * 4;   // [kNB][5][64] fp32 (s, m')
+constexpr int kXStride = 20;                                 // floats per exchange row (padded)
+constexpr int kOffX = kOffA + kNB * kMaxOwn * kPlane;        // [4 quarters][128 rows][kXStride] fp32
+constexpr int kOffMeta = kOffX + 4 * kRows * kXStride * 4;   // [kNB][5][64] fp32 (s, m')
 constexpr int kOffValid = kOffMeta + kNB * kMaxOwn * 64 * 8; // [kNB][2] token masks
 constexpr int kOffSmax = kOffValid + kNB * 2 * 4;            // [kNB][4] largest PV scale per unpack warp
-constexpr int kOffMax = kOffSmax + kNB * 4 * 4;              // [2][2][128] fp32
-constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
+constexpr int kOffMax = kOffSmax + kNB * 4 * 4;              // [2][4][128] fp32
+constexpr int kOffScan = kOffMax + 2 * 4 * kRows * 4;        // [32] int
 constexpr int kOffPages = kOffScan + 32 * 4;                 // [64] page ids of the split
 constexpr int kOffBar = kOffPages + 64 * 4;
 constexpr int kNumBars = 20;
@@ -73,12 +75,12 @@ static_assert(kSmem + 1024 <= 227 * 1024, "shared memory budget (with 1 KB align
 constexpr int kBarAFull = 0;    // [kNB] count 128 (unpack threads)
 constexpr int kBarAFree = 3;    // [kNB] count 1 (issuer commit after the tile's PV)
 constexpr int kBarDFull = 6;    // [2] count 1 (QK commit)
-constexpr int kBarDFree = 8;    // [2] count 256 (softmax threads)
-constexpr int kBarPsFull = 10;  // [2] count 256
+constexpr int kBarDFree = 8;    // [2] count 512 (softmax threads)
+constexpr int kBarPsFull = 10;  // [2] count 512
 constexpr int kBarPsFree = 12;  // [2] count 1 (PV commit)
 constexpr int kBarPV = 14;      // count 1: a tile's PV is complete
 constexpr int kBarXFull = 15;   // count 1 + 32 KB of transactions: the peer's partial logits are in my buffer
-constexpr int kBarXFree = 16;   // count 256: the peer has read its buffer
+constexpr int kBarXFree = 16;   // count 512: the peer has read its buffer
 constexpr int kBarFlush = 17;   // count 1: final drain of the issuer
 
 // tensor memory columns
@@ -102,6 +104,12 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t*
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // 32 consecutive columns of this thread's lane, one wait.
@@ -203,25 +211,25 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int
   }
 }
 
-// OR of `pred` over the 256 softmax threads (named barrier 1).
+// OR of `pred` over the 512 softmax threads (named barrier 1).
 __device__ __forceinline__ bool soft_any(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      " bar.red.or.pred q, 1, 512, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)pred)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-// OR of `pred` over the two softmax warps of TMEM lane quadrant qd (named
-// barrier 2 + qd, 64 threads).
-__device__ __forceinline__ bool pair_any(bool pred, int qd) {
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// OR of `pred` over the four softmax warps of TMEM lane quadrant qd (named
+// barrier 2 + qd, 128 threads).
+__device__ __forceinline__ bool quad_any(bool pred, int qd) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, %2, 64, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      " bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)pred), "r"(2 + qd)
       : "memory");
@@ -502,8 +510,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::bar_arrive(bar(kBarAFull + buf));
     }
   } else if (warp < kIssuerWarp) {
-    // ---------------- softmax: row h (TMEM lane), tokens 32th .. 32th+31
-    const int qd = warp & 3, th = (warp - 4) >> 2, h = 32 * qd + lane;
+    // ---------------- softmax: row h (TMEM lane), tokens kTW*tq .. kTW*tq+kTW-1
+    const int qd = warp & 3, tq = (warp - 4) >> 2, h = 32 * qd + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
     const uint32_t x_peer = map_peer(tc::su32(sX), peer);
     const uint32_t xfull_peer = map_peer(bar(kBarXFull), peer);
@@ -538,9 +546,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int buf = i % kNB;
       const bool packed_tile = i < n_pk;
       const float2* meta = sMeta + buf * kMaxOwn * 64;
-      float S[32];
+      float S[kTW];
 #pragma unroll
-      for (int t = 0; t < 32; ++t) S[t] = 0.f;
+      for (int t = 0; t < kTW; ++t) S[t] = 0.f;
       // fold the partial logits of my groups
 #pragma unroll
       for (int j = 0; j < kMaxOwn; ++j) {
@@ -550,13 +558,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = warp_all(ok);
         if (ok) {
           tc::tc_fence_after();
-          float D[32];
-          tmem_ld32(tl + kColD + 64 * slot + 32 * th, D);
+          float D[kTW];
+          tc::tmem_ld16(tl + kColD + 64 * slot + kTW * tq, D);
           tc::tc_fence_before();
           tc::bar_arrive(bar(kBarDFree + slot));
-          const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64 + 32 * th);
+          const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64 + kTW * tq);
 #pragma unroll
-          for (int t2 = 0; t2 < 16; ++t2) {
+          for (int t2 = 0; t2 < kTW / 2; ++t2) {
             const float4 mv = m4[t2];  // (s, m') of tokens 2 t2, 2 t2 + 1
             S[2 * t2] = fmaf(mv.x, D[2 * t2], fmaf(mv.y, qs[j], S[2 * t2]));
             S[2 * t2 + 1] = fmaf(mv.z, D[2 * t2 + 1], fmaf(mv.w, qs[j], S[2 * t2 + 1]));
@@ -564,22 +572,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++kq;
       }
-      // exchange with the peer: my partial of tokens 32th..32th+31 goes to the
+      // exchange with the peer: my partial of my kTW tokens goes to the
       // peer's buffer (once the peer has read the previous tile's), the peer's
       // partial of the same tokens arrives in mine
       if (ok && i >= 1) ok = bar_wait_cluster(bar(kBarXFree), (i - 1) & 1, abort_flag, a.err);
       if (ok) {
-        const uint32_t dst = x_peer + (uint32_t)((th * kRows + h) * kXStride) * 4u;
+        const uint32_t dst = x_peer + (uint32_t)((tq * kRows + h) * kXStride) * 4u;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < kTW / 4; ++k)
           st_async4(dst + 16 * k, S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3], xfull_peer);
-        if (tid == 128) expect_tx(bar(kBarXFull), kSoftThreads * 32 * 4);
+        if (tid == 128) expect_tx(bar(kBarXFull), kSoftThreads * kTW * 4);
         ok = wait(bar(kBarXFull), i & 1, abort_flag, a.err);
       }
       if (ok) {
-        const float4* src = reinterpret_cast<const float4*>(sX + (th * kRows + h) * kXStride);
+        const float4* src = reinterpret_cast<const float4*>(sX + (tq * kRows + h) * kXStride);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kTW / 4; ++k) {
           const float4 v = src[k];
           S[4 * k] += v.x;
           S[4 * k + 1] += v.y;
@@ -588,20 +596,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         arrive_peer_relaxed(xfree_peer);
       }
-      // validity, log2 scale, tile max over both halves
-      const int tok0 = bf_first + (i - n_pk) * 64 + 32 * th;  // bf16 tiles
-      const uint32_t vmask = sMask[buf * 2 + th];                // packed tiles
+      // validity, log2 scale, tile max over the four quarters
+      const int tok0 = bf_first + (i - n_pk) * 64 + kTW * tq;                   // bf16 tiles
+      const uint32_t vmask = sMask[buf * 2 + (tq >> 1)] >> (kTW * (tq & 1));  // packed tiles
       float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
+      for (int t = 0; t < kTW; ++t) {
         const bool v = packed_tile ? ((vmask >> t) & 1u) != 0
                                    : (tok0 + t < bf_end && tok0 + t < sw.n_tok - n_masked);
         S[t] = v ? S[t] * a.scale_log2 : -INFINITY;
         mx = fmaxf(mx, S[t]);
       }
-      sMax[((i & 1) * 2 + th) * kRows + h] = mx;
-      if (pair_any(!ok, qd)) break;  // both warps of the rows leave at the same tile
-      const float tmax = fmaxf(sMax[((i & 1) * 2) * kRows + h], sMax[((i & 1) * 2 + 1) * kRows + h]);
+      sMax[((i & 1) * 4 + tq) * kRows + h] = mx;
+      if (quad_any(!ok, qd)) break;  // the four warps of the rows leave at the same tile
+      const float tmax = fmaxf(fmaxf(sMax[((i & 1) * 4) * kRows + h], sMax[((i & 1) * 4 + 1) * kRows + h]),
+                               fmaxf(sMax[((i & 1) * 4 + 2) * kRows + h], sMax[((i & 1) * 4 + 3) * kRows + h]));
       // lazy max: moved only when the tile max exceeds it by kLazy, or by less
       // when the tile's largest scale s would take P * s <= 2^kLazy * s past
       // the fp16 range
@@ -621,8 +630,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) accm[j] *= alpha;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t col = kColO + 128 * th + 32 * c;
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t col = kColO + 64 * tq + 32 * c;
             float v[32];
             tmem_ld32(tl + col, v);
 #pragma unroll
@@ -634,7 +643,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       m_run = m_new;
       float lsum = 0.f;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
+      for (int t = 0; t < kTW; ++t) {
         S[t] = S[t] == -INFINITY ? 0.f : fast_exp2(S[t] - m_run);
         lsum += S[t];
       }
@@ -647,19 +656,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = warp_all(ok);
         if (!ok) continue;
         tc::tc_fence_after();
-        const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64 + 32 * th);
-        uint32_t hi[16], lo[16];
+        const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64 + kTW * tq);
+        uint32_t hi[kTW / 2], lo[kTW / 2];
         float am = 0.f;
 #pragma unroll
-        for (int t2 = 0; t2 < 16; ++t2) {
+        for (int t2 = 0; t2 < kTW / 2; ++t2) {
           const float4 mv = m4[t2];  // (s, m') of tokens 2 t2, 2 t2 + 1
           const float p0 = S[2 * t2], p1 = S[2 * t2 + 1];
           am = fmaf(p0, mv.y, fmaf(p1, mv.w, am));
           split_trunc(p0 * mv.x, p1 * mv.z, hi[t2], lo[t2]);
         }
         accm[j] += am;
-        tmem_st16_nowait(tl + kColPs + 64 * pslot + 16 * th, hi);
-        tmem_st16_nowait(tl + kColPs + 64 * pslot + 32 + 16 * th, lo);
+        tmem_st8_nowait(tl + kColPs + 64 * pslot + (kTW / 2) * tq, hi);
+        tmem_st8_nowait(tl + kColPs + 64 * pslot + 32 + (kTW / 2) * tq, lo);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc::tc_fence_before();
         tc::bar_arrive(bar(kBarPsFull + pslot));
@@ -672,20 +681,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool done = ok && n_tiles > 0 && done_tiles == n_tiles &&
                 wait(bar(kBarPV), (n_tiles - 1) & 1, abort_flag, a.err);
     done = !soft_any(!done);  // one decision for all softmax warps
-    sX[(th * 5) * kRows + h] = l;
+    sX[(tq * 5) * kRows + h] = l;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) sX[(th * 5 + 1 + j) * kRows + h] = accm[j];
+    for (int j = 0; j < 4; ++j) sX[(tq * 5 + 1 + j) * kRows + h] = accm[j];
     soft_sync();
-    const float l_tot = sX[h] + sX[5 * kRows + h];
-    float mt[4];
+    float l_tot = 0.f, mt[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mt[j] = sX[(1 + j) * kRows + h] + sX[(6 + j) * kRows + h];
+    for (int k = 0; k < 4; ++k) {
+      l_tot += sX[(k * 5) * kRows + h];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mt[j] += sX[(k * 5 + 1 + j) * kRows + h];
+    }
     float* orow = a.part_o + ((long long)sidx * a.H + h) * kLatent;
     if (done) {
       tc::tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const int col = 128 * th + 32 * c;
+      for (int c = 0; c < 2; ++c) {
+        const int col = 64 * tq + 32 * c;
         float v[32];
         tmem_ld32(tl + kColO + col, v);
         const int j = col >> 6, g = 4 * r + j;
@@ -695,13 +707,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           orow[g * 64 + tc::chan_of_pos(cc >> 3, cc & 7, kTypeB)] = v[e] + mt[j];
         }
       }
-      if (r == 0 && th == 0) {
+      if (r == 0 && tq == 0) {
         a.part_ml[((long long)sidx * a.H + h) * 2] = m_run;
         a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = l_tot;
       }
     } else {
-      for (int c = 0; c < 128; ++c) orow[(4 * r + 2 * th) * 64 + c] = 0.f;
-      if (r == 0 && th == 0) {
+      for (int c = 0; c < 64; ++c) orow[(4 * r + tq) * 64 + c] = 0.f;
+      if (r == 0 && tq == 0) {
         a.part_ml[((long long)sidx * a.H + h) * 2] = -INFINITY;
         a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = 0.f;
       }
