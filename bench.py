@@ -540,16 +540,17 @@ def run_table9(args):
 
 def run_mtp(args):
     """Multi-token query decode on the v2lite shape (B8 H16 L32768 C4R4): decode
-    time for 1, 2 and 4 causal queries per sequence over the same cache (the
+    time for 1, 2, 4 and 8 causal queries per sequence over the same cache (the
     Group-Query Latent Attention abstract's s_q = 2 multi-token prediction
-    step). One JSON line per query count; L2 flushed before each timed call."""
+    step; 8 queries of 16 heads are 128 rows, which the 2-CTA tcgen05 kernel
+    takes). One JSON line per query count; L2 flushed before each timed call."""
     import torch
     w = syn.get("v2lite_c4r4")
     s = Setup(w, "cuda:0")
     peak, peak_kind = peaks()
     tpk, tpk_kind = tensor_peak()
     base = None
-    for n in (1, 2, 4):
+    for n in (1, 2, 4, 8):
         g = torch.Generator(device="cuda")
         g.manual_seed(100 + n)
         q = torch.randn(w.batch, n, w.heads, 576, generator=g, device="cuda").to(torch.bfloat16)

@@ -177,3 +177,25 @@ def test_plan_fills_one_wave_on_uniform_lengths():
     # ceil(4152 / 152) = 28 -> 19 splits per sequence: one wave of 152 CTAs
     total, chunk, _ = pkg.decode_plan(pkg.layout(4, 4), 16, [32768] * 8, num_sms=152)
     assert (total, chunk) == (152, 28)
+
+
+def test_plan_spreads_work_over_full_waves():
+    # one CTA per SM; 128 heads run as 2-CTA clusters.  The planner picks the
+    # fewest waves the 64-page cap allows, then the smallest chunk whose splits
+    # fit those waves, so the last wave is not a short tail.
+    lay = pkg.layout(4, 4)
+    for heads, lens in [(128, [8192] * 32), (128, [131072] * 4), (128, [10240] * 32),
+                        (16, [2000] * 1000), (16, [32768] * 8)]:
+        total, chunk, _ = pkg.decode_plan(lay, heads, lens, num_sms=152)
+        cps = 2 if heads == 128 else heads // 16
+        assert 1 <= chunk <= 64
+        waves = -(-total * cps // 152)
+        capped = sum(_expected_splits(L, True, 64) for L in lens)
+        assert waves == -(-capped * cps // 152) or waves == -(-total * cps // 152)
+        assert waves >= -(-capped * cps // 152)          # never fewer than possible
+        if chunk > 1:                                      # smallest chunk for these waves
+            smaller = sum(_expected_splits(L, True, chunk - 1) for L in lens)
+            assert smaller * cps > waves * 152
+    # the two cases that motivated it
+    assert pkg.decode_plan(lay, 128, [8192] * 32, num_sms=152)[:2] == (128, 34)
+    assert pkg.decode_plan(lay, 128, [131072] * 4, num_sms=152)[:2] == (152, 55)
