@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     LibraryError,
     bytes_per_token,
     decode,
+    decode_multi,
     decode_noalloc,
     decode_plan,
     layout,
@@ -19,5 +20,6 @@ from .binding import (  # noqa: F401
     strerror,
     version,
     write,
+    write_decode,
 )
 from .cache import PagedCache  # noqa: F401
