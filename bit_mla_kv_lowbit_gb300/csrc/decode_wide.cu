@@ -3,38 +3,43 @@
 // 2-CTA cluster per split, for packed caches.
 //
 // Same arithmetic as decode.cu (QuantMLA, Abstract and Figure 8 caption:
-// exact integer codes on the tensor cores, fp32 per-group scale and min folded
-// outside them, P*scale split into fp16 high and low parts for PV, one
-// softmax over all valid tokens).  With 128 rows the heads fill the M = 128
-// dimension of a tcgen05 MMA, so every contraction runs there:
+// exact integer codes on the tensor cores, per-group fp16 scale and min, one
+// softmax over all valid tokens), laid out so that both contractions run on
+// tcgen05 with 128 rows as M:
 //
 // * The two CTAs of a cluster split the channels.  Rank r owns content groups
-//   4r..4r+3 (and rank 1 the RoPE group): it holds q for those channels in
-//   shared memory, unpacks only those groups of each page, and computes the
-//   partial logits sum_g s_g (q_g . c_g) + m'_g sum(q_g) over them (QK: M=128
-//   rows, N=64 tokens, K=16 per MMA; one TMEM accumulator per group, folded
-//   by the softmax warps).  The partials are exchanged through distributed
-//   shared memory, so both CTAs hold the same logits and run the same online
-//   softmax.
-// * Rank r then accumulates O for its 256 output channels: per group, A =
-//   P*s_g (fp16 high and low) written by the softmax warps straight into
-//   tensor memory, B = the group's code plane read as an MN-major operand.
-//   The A operand never passes through shared memory, which is what bounds
-//   small-N MMAs whose A comes from there.
-// * O (128 x 256 fp32) lives in tensor memory for the whole split and is
+//   4r..4r+3 and RoPE channels 32r..32r+31: it unpacks only those parts of
+//   each page (so both ranks carry the same work) and owns output channels
+//   256r..256r+255.
+// * The scale is carried by the B operand.  Each code c (centred) is written
+//   twice, as s_hi * c and s_lo * c, where s_hi is the fp16 scale cut to 7
+//   significant bits and s_lo the exact remainder (at most 4 bits): both
+//   products are exact in fp16.  So QK accumulates every group of a tile into
+//   one tensor-memory accumulator (q . (s c) = q . (s_hi c) + q . (s_lo c)),
+//   and PV runs with one operand P for all groups of the CTA (N = 256):
+//   O += P_hi (s_hi c) + P_lo (s_hi c) + P_hi (s_lo c), with P split into fp16
+//   high and low parts once per row and token.  The min terms (m' = m + centre
+//   s) are rank-one sums done in fp32 on the CUDA cores.  A token whose scale
+//   would take s c past the fp16 range has both planes scaled by 2^-4 and its
+//   logit and P scaled back by 2^4 (exact powers of two).
+// * q of the content groups lives in tensor memory and is the A operand of
+//   QK; the partial logits cross the cluster with st.async into the peer's
+//   shared memory (the sum is commutative, so both CTAs hold bit-identical
+//   logits and make the same online-softmax decisions); P is written by the
+//   softmax warps straight into tensor memory as the A operand of PV; O
+//   (128 x 256 fp32) stays in tensor memory for the whole split and is
 //   rescaled only when a row's running max grows by more than kLazy.
 //
-// Warp roles (672 threads, one CTA per SM):
-//   warps 0-3   unpack: packed bytes -> fp16 code planes and metadata; the
-//               next tile's bytes are loaded into registers while a plane
-//               buffer is still in use;
-//   warps 4-19  softmax: TMEM lane quadrant w & 3 (32 rows), token quarter
-//               (w - 4) >> 2 (16 tokens); fold, exchange, softmax, P*s
-//               operands;
-//   warp 20     MMA issue (one lane) and the TMEM allocation.
+// Warp roles (416 threads, one CTA per SM):
+//   warps 0-3   unpack: two threads per token of the tile (one per half of the
+//               CTA's groups); the next tile's bytes are loaded into registers
+//               while a plane buffer drains;
+//   warps 4-11  softmax: TMEM lane quadrant w & 3 (32 rows), token half
+//               (w - 4) >> 2 (32 tokens);
+//   warp 12     MMA issue (one lane) and the TMEM allocation.
 // Every wait is bounded; on a time-out the CTA records MLA_LOWBIT_DEV_PIPELINE,
-// the softmax warps leave the tile loop together (barrier reduction), the
-// partial is written empty, and tensor memory is still freed.
+// the softmax warps of a quadrant leave the tile loop together, the partial is
+// written empty, and tensor memory is still freed.
 #include "decode_common.cuh"
 #include "tc_util.cuh"
 
@@ -42,51 +47,56 @@ namespace mlalb {
 namespace wide {
 
 constexpr int kRows = 128;
-constexpr int kThreads = 672;
-constexpr int kSoftThreads = 512;
-constexpr int kTW = 16;                 // tokens of a tile per softmax warp
-constexpr int kIssuerWarp = 20;
-constexpr int kNB = 2;                  // code-plane ring depth (tiles)
+constexpr int kThreads = 416;
+constexpr int kUnpackThreads = 128;
+constexpr int kSoftWarp0 = 4;
+constexpr int kSoftThreads = 256;
+constexpr int kIssuerWarp = 12;
+constexpr int kTW = 32;                 // tokens of a tile per softmax warp
+constexpr int kNB = 2;                  // plane-set ring depth (tiles)
 constexpr int kMaxOwn = 5;              // QK groups of a CTA
 constexpr int kPlane = 64 * 128;        // 64 tokens x 64 fp16 (128-byte rows)
+constexpr int kABuf = 2 * kMaxOwn * kPlane;  // s_hi planes of the 5 groups, then s_lo planes
 constexpr int kQBlock = kRows * 128;    // 128 rows x 64 fp16
 constexpr float kLazy = 8.0f;           // log2 units
+constexpr float kShiftAbove = 32768.f;  // |s c| bound beyond which a token's planes are scaled by 2^-4
 
 // shared memory (bytes, from a 1 KB aligned base)
-constexpr int kOffQ = 0;                                     // [5] q blocks
-constexpr int kOffA = kOffQ + kMaxOwn * kQBlock;             // [kNB][5] planes
-constexpr int kXStride = 20;                                 // floats per exchange row (padded)
-constexpr int kOffX = kOffA + kNB * kMaxOwn * kPlane;        // [4 quarters][128 rows][kXStride] fp32
-constexpr int kOffMeta = kOffX + 4 * kRows * kXStride * 4;   // [kNB][5][64] fp32 (s, m')
-constexpr int kOffValid = kOffMeta + kNB * kMaxOwn * 64 * 8; // [kNB][2] token masks
-constexpr int kOffSmax = kOffValid + kNB * 2 * 4;            // [kNB][4] largest PV scale per unpack warp
-constexpr int kOffMax = kOffSmax + kNB * 4 * 4;              // [2][4][128] fp32
-constexpr int kOffScan = kOffMax + 2 * 4 * kRows * 4;        // [32] int
+constexpr int kOffA = 0;                                     // [kNB] plane sets
+constexpr int kOffQR = kOffA + kNB * kABuf;                  // RoPE q block
+constexpr int kXStride = 36;                                 // floats per exchange row (padded)
+constexpr int kOffX = kOffQR + kQBlock;                      // [2 halves][128 rows][kXStride] fp32
+constexpr int kOffMeta = kOffX + 2 * kRows * kXStride * 4;   // [kNB][5][64] fp32 m'
+constexpr int kOffShift = kOffMeta + kNB * kMaxOwn * 64 * 4; // [kNB][64] fp32 token factor
+constexpr int kOffValid = kOffShift + kNB * 64 * 4;          // [kNB][4] 16-token masks
+constexpr int kOffMax = kOffValid + kNB * 4 * 4;             // [2][2][128] fp32
+constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
 constexpr int kOffPages = kOffScan + 32 * 4;                 // [64] page ids of the split
 constexpr int kOffBar = kOffPages + 64 * 4;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 25;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
 constexpr int kSmem = kOffMisc + 64;
-static_assert(kOffA % 1024 == 0 && kPlane % 1024 == 0, "swizzled operands need 1 KB alignment");
+static_assert(kOffQR % 1024 == 0 && kPlane % 1024 == 0, "swizzled operands need 1 KB alignment");
 static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory budget (with 1 KB alignment slack)");
 
 // mbarriers
 constexpr int kBarAFull = 0;    // [kNB] count 128 (unpack threads)
-constexpr int kBarAFree = 3;    // [kNB] count 1 (issuer commit after the tile's PV)
-constexpr int kBarDFull = 6;    // [2] count 1 (QK commit)
-constexpr int kBarDFree = 8;    // [2] count 512 (softmax threads)
-constexpr int kBarPsFull = 10;  // [2] count 512
-constexpr int kBarPsFree = 12;  // [2] count 1 (PV commit)
-constexpr int kBarPV = 14;      // count 1: a tile's PV is complete
-constexpr int kBarXFull = 15;   // count 1 + 32 KB of transactions: the peer's partial logits are in my buffer
-constexpr int kBarXFree = 16;   // count 512: the peer has read its buffer
-constexpr int kBarFlush = 17;   // count 1: final drain of the issuer
+constexpr int kBarAFree = 2;    // [kNB] count 1 (issuer commit after the tile's PV)
+constexpr int kBarDFull = 4;    // count 1: the tile's QK is complete
+constexpr int kBarDFree = 5;    // count 256: the softmax warps have read it
+constexpr int kBarPFull = 6;    // count 256: P of the tile is in tensor memory
+constexpr int kBarPFree = 7;    // count 1: the tile's PV is complete
+constexpr int kBarFlush = 8;    // count 1: final drain of the issuer
+constexpr int kBarXFull = 9;    // [8] per softmax warp w: count 1 + 4 KB of transactions, the peer's
+                                //     warp w has written its partial logits into my buffer
+constexpr int kBarXFree = 17;   // [8] per softmax warp w: count 1, the peer's warp w has read its buffer
 
 // tensor memory columns
-constexpr uint32_t kColO = 0;     // [4 groups][64 channels]
-constexpr uint32_t kColD = 256;   // [2 slots][64 tokens] QK accumulators
-constexpr uint32_t kColPs = 384;  // [2 slots][hi 32 | lo 32] P*s operands (fp16 pairs)
+constexpr uint32_t kColO = 0;     // [4 groups][64 channels] fp32
+constexpr uint32_t kColD = 256;   // [64 tokens] fp32 QK accumulator
+constexpr uint32_t kColP = 320;   // [hi 32 | lo 32] fp16 pairs: P of 64 tokens
+constexpr uint32_t kColQ = 384;   // [4 content groups][32] fp16 pairs: q
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
@@ -95,6 +105,15 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* v) {
@@ -202,25 +221,25 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int
   }
 }
 
-// OR of `pred` over the 512 softmax threads (named barrier 1).
+// OR of `pred` over the 256 softmax threads (named barrier 1).
 __device__ __forceinline__ bool soft_any(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, 1, 512, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      " bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)pred)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
-// OR of `pred` over the four softmax warps of TMEM lane quadrant qd (named
-// barrier 2 + qd, 128 threads).
-__device__ __forceinline__ bool quad_any(bool pred, int qd) {
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// OR of `pred` over the two softmax warps of TMEM lane quadrant qd (named
+// barrier 2 + qd, 64 threads).
+__device__ __forceinline__ bool pair_any(bool pred, int qd) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      " bar.red.or.pred q, %2, 64, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)pred), "r"(2 + qd)
       : "memory");
@@ -239,23 +258,46 @@ __device__ __forceinline__ void split_trunc(float a, float b, uint32_t& hi, uint
   lo = pack_half2(a - ha, b - hb);
 }
 
-// Global group of local QK group j of rank r.
-__device__ __forceinline__ int group_of(int r, int j) { return j < 4 ? 4 * r + j : 8; }
+// fp16 bits of the two parts of a scale: hi keeps 7 significant bits, lo is the
+// exact remainder (at most 4 bits); both scaled by 2^-4 when `shift`.
+__device__ __forceinline__ void scale_parts(uint32_t s16, bool shift, uint32_t& hi2, uint32_t& lo2) {
+  const __half s = __ushort_as_half((unsigned short)s16);
+  const __half hi = __ushort_as_half((unsigned short)(s16 & 0xFFF0u));
+  __half lo = __hsub(s, hi);
+  __half h2 = hi;
+  if (shift) {
+    h2 = __hmul(hi, __float2half(0.0625f));
+    lo = __hmul(lo, __float2half(0.0625f));
+  }
+  hi2 = (uint32_t)__half_as_ushort(h2) * 0x00010001u;
+  lo2 = (uint32_t)__half_as_ushort(lo) * 0x00010001u;
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Channel position (0..63, chunk-major) -> channel of the group, for a plane or
+// q row in the unpack's order.
+__device__ __forceinline__ int chan_at(int p, bool tb) { return tc::chan_of_pos(p >> 3, p & 7, tb); }
 
 template <int CB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_wide_kernel(DecodeArgs a) {
   constexpr bool kTypeB = CB == 2;
   constexpr PageGeom G = page_geom(CB);
+  constexpr float kCentreC = kTypeB ? float(kCentre2) : float(kCentre4);
+  constexpr float kCmaxC = kTypeB ? 2.f : 8.f;  // largest |code - centre| of a content group
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::su32(smem_raw) & 1023)) & 1023);
-  uint8_t* sQ = smem + kOffQ;
   uint8_t* sA = smem + kOffA;
+  uint8_t* sQR = smem + kOffQR;
   float* sX = reinterpret_cast<float*>(smem + kOffX);
-  float2* sMeta = reinterpret_cast<float2*>(smem + kOffMeta);
+  float* sMeta = reinterpret_cast<float*>(smem + kOffMeta);
+  float* sShift = reinterpret_cast<float*>(smem + kOffShift);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + kOffValid);
   float* sMax = reinterpret_cast<float*>(smem + kOffMax);
-  float* sSmax = reinterpret_cast<float*>(smem + kOffSmax);
   int* scan = reinterpret_cast<int*>(smem + kOffScan);
   int* s_pages = reinterpret_cast<int*>(smem + kOffPages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -286,21 +328,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n_tiles = n_pk + max(0, (bf_end - bf_first + 63) / 64);
   const int n_own = 4 + r;
 
-  // ---- set-up: barriers, TMEM, q blocks
+  // ---- set-up: barriers, TMEM, page ids, RoPE q block
   if (tid == 0) {
     for (int i = 0; i < kNB; ++i) {
-      tc::bar_init(bar(kBarAFull + i), 128);
+      tc::bar_init(bar(kBarAFull + i), kUnpackThreads);
       tc::bar_init(bar(kBarAFree + i), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      tc::bar_init(bar(kBarDFull + s), 1);
-      tc::bar_init(bar(kBarDFree + s), kSoftThreads);
-      tc::bar_init(bar(kBarPsFull + s), kSoftThreads);
-      tc::bar_init(bar(kBarPsFree + s), 1);
+    tc::bar_init(bar(kBarDFull), 1);
+    tc::bar_init(bar(kBarDFree), kSoftThreads);
+    tc::bar_init(bar(kBarPFull), kSoftThreads);
+    tc::bar_init(bar(kBarPFree), 1);
+    for (int w = 0; w < kSoftThreads / 32; ++w) {
+      tc::bar_init(bar(kBarXFull + w), 1);
+      tc::bar_init(bar(kBarXFree + w), 1);
     }
-    tc::bar_init(bar(kBarPV), 1);
-    tc::bar_init(bar(kBarXFull), 1);
-    tc::bar_init(bar(kBarXFree), kSoftThreads);
     tc::bar_init(bar(kBarFlush), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -311,48 +352,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // q block j: row h, chunk c holds the group's channels in the unpack's order
-  for (int u = tid; u < n_own * kRows * 4; u += kThreads) {
-    const int j = u / (kRows * 4), h = (u >> 2) % kRows, cc = u & 3;
-    const int g = group_of(r, j);
-    const bool tb = g < 8 && kTypeB;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        a.q + ((long long)b * a.H + h) * kDim + g * 64 + 16 * cc);
-    const uint4 v0 = src[0], v1 = src[1];
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int c = 2 * cc + c2;
-      uint32_t o[4];
-#pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) {
-        const int p0 = tc::chan_of_pos(c, 2 * e2, tb) - 16 * cc;
-        const int p1 = tc::chan_of_pos(c, 2 * e2 + 1, tb) - 16 * cc;
-        const float f0 = (p0 & 1) ? bf16hi_to_f32(w[p0 >> 1]) : bf16lo_to_f32(w[p0 >> 1]);
-        const float f1 = (p1 & 1) ? bf16hi_to_f32(w[p1 >> 1]) : bf16lo_to_f32(w[p1 >> 1]);
-        o[e2] = pack_half2(f0, f1);
-      }
-      *reinterpret_cast<uint4*>(sQ + j * kQBlock + tc::sw_chunk(h, c)) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
   // page ids of the split's packed pages (the planner caps a split at 64)
   for (int k = tid; k < min(n_pk, 64); k += kThreads)
     s_pages[k] = a.block_table[(long long)b * a.max_pages + sw.page_begin + k];
+  // RoPE q block: row h, chunk c holds the channels in the unpack's order (each
+  // rank multiplies only its half of them)
+  {
+    for (int u = tid; u < kRows * 4; u += kThreads) {
+      const int h = u >> 2, cc = u & 3;
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((long long)b * a.H + h) * kDim + 512 + 16 * cc);
+      const uint4 v0 = src[0], v1 = src[1];
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = 2 * cc + c2;
+        uint32_t o[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int p0 = tc::chan_of_pos(c, 2 * e2, false) - 16 * cc;
+          const int p1 = tc::chan_of_pos(c, 2 * e2 + 1, false) - 16 * cc;
+          const float f0 = (p0 & 1) ? bf16hi_to_f32(w[p0 >> 1]) : bf16lo_to_f32(w[p0 >> 1]);
+          const float f1 = (p1 & 1) ? bf16hi_to_f32(w[p1 >> 1]) : bf16lo_to_f32(w[p1 >> 1]);
+          o[e2] = pack_half2(f0, f1);
+        }
+        *reinterpret_cast<uint4*>(sQR + tc::sw_chunk(h, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
   tc::fence_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before any remote arrive or store
   const uint32_t tmem = *tmem_slot;
 
+  // softmax warps: q of content groups 2th, 2th+1 into tensor memory (row h =
+  // lane of quadrant qd), and the group sums of the row's q for the min terms
+  float qs[kMaxOwn] = {0.f, 0.f, 0.f, 0.f, 0.f};
+  if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 8) {
+    const int qd = warp & 3, th = (warp - kSoftWarp0) >> 2, h = 32 * qd + lane;
+    const uint16_t* qrow = a.q + ((long long)b * a.H + h) * kDim;
+#pragma unroll
+    for (int j = 0; j < kMaxOwn; ++j) {
+      const int g = j < 4 ? 4 * r + j : 8;
+      const bool tb = j < 4 && kTypeB;
+      uint32_t w[32];
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * g);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = src[k];
+        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+      }
+      uint32_t o[32];
+      float acc = 0.f;
+#pragma unroll
+      for (int p2 = 0; p2 < 32; ++p2) {
+        const int c0 = tb ? chan_at(2 * p2, true) : chan_at(2 * p2, false);
+        const int c1 = tb ? chan_at(2 * p2 + 1, true) : chan_at(2 * p2 + 1, false);
+        const float f0 = (c0 & 1) ? bf16hi_to_f32(w[c0 >> 1]) : bf16lo_to_f32(w[c0 >> 1]);
+        const float f1 = (c1 & 1) ? bf16hi_to_f32(w[c1 >> 1]) : bf16lo_to_f32(w[c1 >> 1]);
+        o[p2] = pack_half2(f0, f1);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&o[p2]));
+        acc += hf.x + hf.y;
+      }
+      qs[j] = acc;
+      if (j < 4 && (j >> 1) == th) {
+        const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+        tmem_st8_nowait(tl + kColQ + 32 * j, o);
+        tmem_st8_nowait(tl + kColQ + 32 * j + 8, o + 8);
+        tmem_st8_nowait(tl + kColQ + 32 * j + 16, o + 16);
+        tmem_st8_nowait(tl + kColQ + 32 * j + 24, o + 24);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  cluster_sync();  // the peer's barriers exist before any remote arrive or store
+
   if (warp < 4) {
-    // ---------------- unpack: token t, part pp (local groups 2pp, 2pp+1 and
-    // RoPE channels 32pp..32pp+31 on rank 1)
-    const int t = tid & 63, pp = tid >> 6;
-    // registers of the next packed tile: codes of the thread's two content
-    // groups, its RoPE quarter (rank 1) and the metadata words
-    uint4 nc[4], nr = make_uint4(0, 0, 0, 0);
-    uint32_t nm[3] = {0u, 0u, 0u};
+    // ---------------- unpack: token t of every tile; thread half gh takes
+    // content groups 2gh, 2gh+1 and RoPE words 4r+2gh, 4r+2gh+1 (16 channels)
+    const int t = tid >> 1, gh = tid & 1;
+    uint4 nc[4];
+    uint2 nr = make_uint2(0, 0);
+    uint32_t nm[3];
     bool n_ok = false, n_okt = false;
     auto fetch = [&](int i) {
       const int page_idx = sw.page_begin + i;
@@ -365,410 +449,241 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint8_t* crow = pb + G.content_off + t * G.content_row;
       const uint8_t* mrow = pb + G.meta_off + t * G.meta_row;
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int g = 4 * r + 2 * pp + jj;
-        nc[2 * jj] = nc[2 * jj + 1] = make_uint4(0, 0, 0, 0);
-        nm[jj] = 0u;
-        if (n_ok) {
-          if constexpr (CB == 4) {
-            nc[2 * jj] = *reinterpret_cast<const uint4*>(crow + 32 * g);
-            nc[2 * jj + 1] = *reinterpret_cast<const uint4*>(crow + 32 * g + 16);
-          } else {
-            nc[2 * jj] = *reinterpret_cast<const uint4*>(crow + 16 * g);
-          }
-        }
-        if (n_okt) nm[jj] = *reinterpret_cast<const uint32_t*>(mrow + 4 * g);
+      for (int k = 0; k < 4; ++k) nc[k] = make_uint4(0, 0, 0, 0);
+      nr = make_uint2(0, 0);
+      nm[0] = nm[1] = nm[2] = 0u;
+      if (n_ok) {
+        // groups 4r + 2gh, 4r + 2gh + 1 are contiguous in the row
+        const uint4* cs = reinterpret_cast<const uint4*>(crow + (CB == 4 ? 32 : 16) * (4 * r + 2 * gh));
+#pragma unroll
+        for (int k = 0; k < (CB == 4 ? 4 : 2); ++k) nc[k] = cs[k];
+        nr = *reinterpret_cast<const uint2*>(pb + G.rope_off + t * G.rope_row + 16 * r + 8 * gh);
       }
-      nr = make_uint4(0, 0, 0, 0);
-      nm[2] = 0u;
-      if (r == 1) {
-        if (n_ok) nr = *reinterpret_cast<const uint4*>(pb + G.rope_off + t * G.rope_row + 16 * pp);
-        if (n_okt && pp == 0) nm[2] = *reinterpret_cast<const uint32_t*>(mrow + 32);
+      if (n_okt) {
+        nm[0] = *reinterpret_cast<const uint32_t*>(mrow + 4 * (4 * r + 2 * gh));
+        nm[1] = *reinterpret_cast<const uint32_t*>(mrow + 4 * (4 * r + 2 * gh + 1));
+        nm[2] = *reinterpret_cast<const uint32_t*>(mrow + 32);
       }
     };
     if (n_pk > 0) fetch(0);
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i % kNB;
-      const uint4 cc0 = nc[0], cc1 = nc[1], cc2 = nc[2], cc3 = nc[3], rr = nr;
-      const uint32_t mw0 = nm[0], mw1 = nm[1], mw2 = nm[2];
+      uint4 cc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cc[k] = nc[k];
+      const uint2 rr = nr;
+      const uint32_t mw[3] = {nm[0], nm[1], nm[2]};
       const bool okt_cur = n_okt;
       if (i + 1 < n_pk) fetch(i + 1);  // in flight while the buffer drains
-      if (i >= kNB && !wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err))
-        break;
-      uint8_t* A = sA + buf * kMaxOwn * kPlane;
-      float2* meta = sMeta + buf * kMaxOwn * 64;
-      // (s, m' = m + centre * s) of a metadata word, as the softmax warps use them
-      auto sm_of = [](uint32_t w, float centre) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
-        return make_float2(f.x, fmaf(centre, f.x, f.y));
-      };
+      if (i >= kNB && !wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err)) break;
+      uint8_t* A = sA + buf * kABuf;
+      float* meta = sMeta + buf * kMaxOwn * 64;
+      bool okt;
       if (i < n_pk) {
+        okt = okt_cur;
+        // one factor per token: 2^-4 on both planes when some group's s * |c|
+        // could leave the fp16 range (decided with the token's other half)
+        float smax = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 3; ++jj) {
+          const float s = __half2float(__ushort_as_half((unsigned short)(mw[jj] & 0xFFFFu)));
+          smax = fmaxf(smax, s * (jj < 2 ? kCmaxC : 8.f));
+        }
+        smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
+        const bool shift = smax > kShiftAbove;
+        if (gh == 0) sShift[buf * 64 + t] = shift ? 16.f : 1.f;
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * pp + jj;
-          uint8_t* plane = A + j * kPlane;
-          const uint4 c0 = jj ? cc2 : cc0, c1 = jj ? cc3 : cc1;
+          const int j = 2 * gh + jj;
+          uint32_t hi2, lo2;
+          scale_parts(mw[jj] & 0xFFFFu, shift, hi2, lo2);
+          uint8_t* p1 = A + j * kPlane;
+          uint8_t* p2 = A + (kMaxOwn + j) * kPlane;
+          // the token's two threads write the same positions of planes 8 KB
+          // apart (same banks): the second one walks the chunks in another
+          // order, so that their stores never meet in one bank
           if constexpr (CB == 4) {
+            const uint4 c0 = cc[2 * jj], c1 = cc[2 * jj + 1];
             const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
             for (int k2 = 0; k2 < 8; ++k2) {
+              const int kk = k2 ^ (gh << 2);
               uint32_t p[4];
-              unpack_int4(w[k2], p);
-              *reinterpret_cast<uint4*>(plane + tc::sw_chunk(t, k2)) = make_uint4(p[0], p[1], p[2], p[3]);
+              unpack_int4(gh ? w[k2 ^ 4] : w[k2], p);
+              *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, kk)) =
+                  make_uint4(hmul2u(p[0], hi2), hmul2u(p[1], hi2), hmul2u(p[2], hi2), hmul2u(p[3], hi2));
+              *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, kk)) =
+                  make_uint4(hmul2u(p[0], lo2), hmul2u(p[1], lo2), hmul2u(p[2], lo2), hmul2u(p[3], lo2));
             }
           } else {
+            const uint4 c0 = cc[jj];
             const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
+              const int kk = k2 ^ (gh << 1);
               uint32_t p[8];
-              unpack_int2(w[k2], p);
-              *reinterpret_cast<uint4*>(plane + tc::sw_chunk(t, 2 * k2)) = make_uint4(p[0], p[1], p[2], p[3]);
-              *reinterpret_cast<uint4*>(plane + tc::sw_chunk(t, 2 * k2 + 1)) = make_uint4(p[4], p[5], p[6], p[7]);
+              unpack_int2(gh ? w[k2 ^ 2] : w[k2], p);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 2 * kk + hh)) =
+                    make_uint4(hmul2u(p[4 * hh], hi2), hmul2u(p[4 * hh + 1], hi2),
+                               hmul2u(p[4 * hh + 2], hi2), hmul2u(p[4 * hh + 3], hi2));
+                *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, 2 * kk + hh)) =
+                    make_uint4(hmul2u(p[4 * hh], lo2), hmul2u(p[4 * hh + 1], lo2),
+                               hmul2u(p[4 * hh + 2], lo2), hmul2u(p[4 * hh + 3], lo2));
+              }
             }
           }
-          meta[j * 64 + t] = sm_of(jj ? mw1 : mw0, kTypeB ? float(kCentre2) : float(kCentre4));
+          const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw[jj]));
+          meta[j * 64 + t] = fmaf(kCentreC, sm.x, sm.y);
         }
-        if (r == 1) {
-          const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
-          uint8_t* plane = A + 4 * kPlane;
+        {
+          // RoPE words 4r + 2gh, 4r + 2gh + 1 -> chunks of the same index
+          uint32_t hi2, lo2;
+          scale_parts(mw[2] & 0xFFFFu, shift, hi2, lo2);
+          uint8_t* p1 = A + 4 * kPlane;
+          uint8_t* p2 = A + (kMaxOwn + 4) * kPlane;
+          const uint32_t w[2] = {rr.x, rr.y};
 #pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2) {
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int c = 4 * r + 2 * gh + k2;
             uint32_t p[4];
             unpack_int4(w[k2], p);
-            *reinterpret_cast<uint4*>(plane + tc::sw_chunk(t, 4 * pp + k2)) = make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, c)) =
+                make_uint4(hmul2u(p[0], hi2), hmul2u(p[1], hi2), hmul2u(p[2], hi2), hmul2u(p[3], hi2));
+            *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, c)) =
+                make_uint4(hmul2u(p[0], lo2), hmul2u(p[1], lo2), hmul2u(p[2], lo2), hmul2u(p[3], lo2));
           }
-          if (pp == 0) meta[4 * 64 + t] = sm_of(mw2, float(kCentre4));
+          if (gh == 0) {
+            const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw[2]));
+            meta[4 * 64 + t] = fmaf(float(kCentre4), sm.x, sm.y);
+          }
         }
-        const uint32_t mk = __ballot_sync(0xffffffffu, okt_cur);
-        if (pp == 0 && lane == 0) sMask[buf * 2 + (t >> 5)] = mk;
-        // largest scale of the PV groups in this tile (bounds P * s in fp16)
-        float smx = fmaxf(meta[(2 * pp) * 64 + t].x, meta[(2 * pp + 1) * 64 + t].x);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, o));
-        if (lane == 0) sSmax[buf * 4 + warp] = smx;
       } else {
-        // protected tokens: bf16 values in place of codes, scale 1, min 0
+        // protected tokens: bf16 values as the s_hi plane, zero s_lo plane, min 0
         const int idx = bf_first + (i - n_pk) * 64 + t;
-        const bool okt = idx < bf_end;
+        okt = idx < bf_end;
         const uint16_t* rp = nullptr;
         if (okt) {
           const int pos = bf16_pos(sw, idx);
           rp = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
                            : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
         }
-        auto put16 = [&](uint8_t* plane, const uint16_t* src16, int cc, bool tb) {
-          // channels 16cc..16cc+15 of a group -> chunks 2cc, 2cc+1
+        if (gh == 0) sShift[buf * 64 + t] = 1.f;
+        // 16-channel blocks: 4 per content group (2 groups), then RoPE block 2r + gh
+#pragma unroll 1
+        for (int blk = 0; blk < 9; ++blk) {
+          const int j = blk < 8 ? 2 * gh + (blk >> 2) : 4;
+          const int cc16 = blk < 8 ? (blk & 3) : 2 * r + gh;
+          const int g = j < 4 ? 4 * r + j : 8;
+          const bool tb = j < 4 && kTypeB;
+          uint8_t* p1 = A + j * kPlane;
+          uint8_t* p2 = A + (kMaxOwn + j) * kPlane;
           uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-          if (src16) {
-            v0 = reinterpret_cast<const uint4*>(src16)[0];
-            v1 = reinterpret_cast<const uint4*>(src16)[1];
+          if (rp) {
+            v0 = reinterpret_cast<const uint4*>(rp + g * 64 + 16 * cc16)[0];
+            v1 = reinterpret_cast<const uint4*>(rp + g * 64 + 16 * cc16)[1];
           }
           const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
-            const int c = 2 * cc + c2;
+            const int c = 2 * cc16 + c2;
             uint32_t o[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              const int p0 = tc::chan_of_pos(c, 2 * e2, tb) - 16 * cc;
-              const int p1 = tc::chan_of_pos(c, 2 * e2 + 1, tb) - 16 * cc;
-              const float f0 = (p0 & 1) ? bf16hi_to_f32(w[p0 >> 1]) : bf16lo_to_f32(w[p0 >> 1]);
-              const float f1 = (p1 & 1) ? bf16hi_to_f32(w[p1 >> 1]) : bf16lo_to_f32(w[p1 >> 1]);
+              const int q0 = tc::chan_of_pos(c, 2 * e2, tb) - 16 * cc16;
+              const int q1 = tc::chan_of_pos(c, 2 * e2 + 1, tb) - 16 * cc16;
+              const float f0 = (q0 & 1) ? bf16hi_to_f32(w[q0 >> 1]) : bf16lo_to_f32(w[q0 >> 1]);
+              const float f1 = (q1 & 1) ? bf16hi_to_f32(w[q1 >> 1]) : bf16lo_to_f32(w[q1 >> 1]);
               o[e2] = pack_half2(f0, f1);
             }
-            *reinterpret_cast<uint4*>(plane + tc::sw_chunk(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, c)) = make_uint4(0, 0, 0, 0);
           }
-        };
-#pragma unroll 1
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * pp + jj, g = 4 * r + j;
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc)
-            put16(A + j * kPlane, rp ? rp + g * 64 + 16 * cc : nullptr, cc, kTypeB);
-          meta[j * 64 + t] = make_float2(okt ? 1.f : 0.f, 0.f);  // (s = 1, m = 0)
         }
-        if (r == 1) {
-#pragma unroll 1
-          for (int cc = 2 * pp; cc < 2 * pp + 2; ++cc)
-            put16(A + 4 * kPlane, rp ? rp + 512 + 16 * cc : nullptr, cc, false);
-          if (pp == 0) meta[4 * 64 + t] = make_float2(okt ? 1.f : 0.f, 0.f);
-        }
-        const uint32_t mk = __ballot_sync(0xffffffffu, okt);
-        if (pp == 0 && lane == 0) sMask[buf * 2 + (t >> 5)] = mk;
-        if (lane == 0) sSmax[buf * 4 + warp] = 1.f;
+        meta[(2 * gh) * 64 + t] = 0.f;
+        meta[(2 * gh + 1) * 64 + t] = 0.f;
+        if (gh == 0) meta[4 * 64 + t] = 0.f;
       }
+      // validity of the warp's 16 tokens (lanes 2k and 2k+1 hold token k)
+      uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
+      mk = (mk | (mk >> 1)) & 0x33333333u;
+      mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
+      mk = (mk | (mk >> 4)) & 0x00FF00FFu;
+      mk = (mk | (mk >> 8)) & 0x0000FFFFu;
+      if (lane == 0) sMask[buf * 4 + warp] = mk;
       tc::fence_async_smem();
       tc::bar_arrive(bar(kBarAFull + buf));
     }
-  } else if (warp < kIssuerWarp) {
-    // ---------------- softmax: row h (TMEM lane), tokens kTW*tq .. kTW*tq+kTW-1
-    const int qd = warp & 3, tq = (warp - 4) >> 2, h = 32 * qd + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
-    const uint32_t x_peer = map_peer(tc::su32(sX), peer);
-    const uint32_t xfull_peer = map_peer(bar(kBarXFull), peer);
-    const uint32_t xfree_peer = map_peer(bar(kBarXFree), peer);
-    // group sums of this row's q (fp16 values, as the MMA sees them)
-    float qs[kMaxOwn];
-#pragma unroll
-    for (int j = 0; j < kMaxOwn; ++j) {
-      float acc = 0.f;
-      if (j < n_own) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(sQ + j * kQBlock + tc::sw_chunk(h, c));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-            acc += f.x + f.y;
-          }
-        }
-      }
-      qs[j] = acc;
-    }
-    // rows of query block qb see all but the last n_q - 1 - qb protected tokens
-    const int n_masked = a.n_q - 1 - h / (kRows / a.n_q);
-    float m_run = -INFINITY, l = 0.f;
-    float accm[4] = {0.f, 0.f, 0.f, 0.f};
-    bool ok = true;
-    int kq = 0;
-    int done_tiles = 0;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int buf = i % kNB;
-      const bool packed_tile = i < n_pk;
-      const float2* meta = sMeta + buf * kMaxOwn * 64;
-      float S[kTW];
-#pragma unroll
-      for (int t = 0; t < kTW; ++t) S[t] = 0.f;
-      // fold the partial logits of my groups
-#pragma unroll
-      for (int j = 0; j < kMaxOwn; ++j) {
-        if (j >= n_own) break;
-        const int slot = kq & 1;
-        if (ok) ok = wait(bar(kBarDFull + slot), (kq >> 1) & 1, abort_flag, a.err);
-        ok = warp_all(ok);
-        if (ok) {
-          tc::tc_fence_after();
-          float D[kTW];
-          tc::tmem_ld16(tl + kColD + 64 * slot + kTW * tq, D);
-          tc::tc_fence_before();
-          tc::bar_arrive(bar(kBarDFree + slot));
-          const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64 + kTW * tq);
-#pragma unroll
-          for (int t2 = 0; t2 < kTW / 2; ++t2) {
-            const float4 mv = m4[t2];  // (s, m') of tokens 2 t2, 2 t2 + 1
-            S[2 * t2] = fmaf(mv.x, D[2 * t2], fmaf(mv.y, qs[j], S[2 * t2]));
-            S[2 * t2 + 1] = fmaf(mv.z, D[2 * t2 + 1], fmaf(mv.w, qs[j], S[2 * t2 + 1]));
-          }
-        }
-        ++kq;
-      }
-      // exchange with the peer: my partial of my kTW tokens goes to the
-      // peer's buffer (once the peer has read the previous tile's), the peer's
-      // partial of the same tokens arrives in mine
-      if (ok && i >= 1) ok = bar_wait_cluster(bar(kBarXFree), (i - 1) & 1, abort_flag, a.err);
-      if (ok) {
-        const uint32_t dst = x_peer + (uint32_t)((tq * kRows + h) * kXStride) * 4u;
-#pragma unroll
-        for (int k = 0; k < kTW / 4; ++k)
-          st_async4(dst + 16 * k, S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3], xfull_peer);
-        if (tid == 128) expect_tx(bar(kBarXFull), kSoftThreads * kTW * 4);
-        ok = wait(bar(kBarXFull), i & 1, abort_flag, a.err);
-      }
-      if (ok) {
-        const float4* src = reinterpret_cast<const float4*>(sX + (tq * kRows + h) * kXStride);
-#pragma unroll
-        for (int k = 0; k < kTW / 4; ++k) {
-          const float4 v = src[k];
-          S[4 * k] += v.x;
-          S[4 * k + 1] += v.y;
-          S[4 * k + 2] += v.z;
-          S[4 * k + 3] += v.w;
-        }
-        arrive_peer_relaxed(xfree_peer);
-      }
-      // validity, log2 scale, tile max over the four quarters
-      const int tok0 = bf_first + (i - n_pk) * 64 + kTW * tq;                   // bf16 tiles
-      const uint32_t vmask = sMask[buf * 2 + (tq >> 1)] >> (kTW * (tq & 1));  // packed tiles
-      float mx = -INFINITY;
-#pragma unroll
-      for (int t = 0; t < kTW; ++t) {
-        const bool v = packed_tile ? ((vmask >> t) & 1u) != 0
-                                   : (tok0 + t < bf_end && tok0 + t < sw.n_tok - n_masked);
-        S[t] = v ? S[t] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, S[t]);
-      }
-      sMax[((i & 1) * 4 + tq) * kRows + h] = mx;
-      if (quad_any(!ok, qd)) break;  // the four warps of the rows leave at the same tile
-      const float tmax = fmaxf(fmaxf(sMax[((i & 1) * 4) * kRows + h], sMax[((i & 1) * 4 + 1) * kRows + h]),
-                               fmaxf(sMax[((i & 1) * 4 + 2) * kRows + h], sMax[((i & 1) * 4 + 3) * kRows + h]));
-      // lazy max: moved only when the tile max exceeds it by kLazy, or by less
-      // when the tile's largest scale s would take P * s <= 2^kLazy * s past
-      // the fp16 range
-      const float smax = fmaxf(fmaxf(sSmax[buf * 4], sSmax[buf * 4 + 1]),
-                               fmaxf(sSmax[buf * 4 + 2], sSmax[buf * 4 + 3]));
-      const float lim = smax > 0.f ? fmaxf(0.f, fminf(kLazy, log2f(32768.f / smax))) : kLazy;
-      const bool need = m_run != -INFINITY && tmax > m_run + lim;
-      const float m_new = (m_run == -INFINITY || need) ? tmax : m_run;
-      if (__any_sync(0xffffffffu, need)) {
-        // rescale what PV has accumulated so far (previous tile's PV done)
-        if (ok) ok = wait(bar(kBarPV), (i - 1) & 1, abort_flag, a.err);
-        ok = warp_all(ok);
-        if (ok) {
-          tc::tc_fence_after();
-          const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-          l *= alpha;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) accm[j] *= alpha;
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t col = kColO + 64 * tq + 32 * c;
-            float v[32];
-            tmem_ld32(tl + col, v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] *= alpha;
-            tmem_st32(tl + col, v);
-          }
-        }
-      }
-      m_run = m_new;
-      float lsum = 0.f;
-#pragma unroll
-      for (int t = 0; t < kTW; ++t) {
-        S[t] = S[t] == -INFINITY ? 0.f : fast_exp2(S[t] - m_run);
-        lsum += S[t];
-      }
-      l += lsum;
-      // P * s_j operands of my four PV groups, high and low fp16 parts
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int kp = 4 * i + j, pslot = kp & 1;
-        if (ok && kp >= 2) ok = wait(bar(kBarPsFree + pslot), ((kp >> 1) - 1) & 1, abort_flag, a.err);
-        ok = warp_all(ok);
-        if (!ok) continue;
-        tc::tc_fence_after();
-        const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64 + kTW * tq);
-        uint32_t hi[kTW / 2], lo[kTW / 2];
-        float am = 0.f;
-#pragma unroll
-        for (int t2 = 0; t2 < kTW / 2; ++t2) {
-          const float4 mv = m4[t2];  // (s, m') of tokens 2 t2, 2 t2 + 1
-          const float p0 = S[2 * t2], p1 = S[2 * t2 + 1];
-          am = fmaf(p0, mv.y, fmaf(p1, mv.w, am));
-          split_trunc(p0 * mv.x, p1 * mv.z, hi[t2], lo[t2]);
-        }
-        accm[j] += am;
-        tmem_st8_nowait(tl + kColPs + 64 * pslot + (kTW / 2) * tq, hi);
-        tmem_st8_nowait(tl + kColPs + 64 * pslot + 32 + (kTW / 2) * tq, lo);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc::tc_fence_before();
-        tc::bar_arrive(bar(kBarPsFull + pslot));
-      }
-      done_tiles = i + 1;
-    }
-    // ---- epilogue: halves' l and min terms through the exchange buffer (no
-    // more traffic from the peer), then my 128 output columns
-    soft_sync();
-    bool done = ok && n_tiles > 0 && done_tiles == n_tiles &&
-                wait(bar(kBarPV), (n_tiles - 1) & 1, abort_flag, a.err);
-    done = !soft_any(!done);  // one decision for all softmax warps
-    sX[(tq * 5) * kRows + h] = l;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) sX[(tq * 5 + 1 + j) * kRows + h] = accm[j];
-    soft_sync();
-    float l_tot = 0.f, mt[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      l_tot += sX[(k * 5) * kRows + h];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mt[j] += sX[(k * 5 + 1 + j) * kRows + h];
-    }
-    float* orow = a.part_o + ((long long)sidx * a.H + h) * kLatent;
-    if (done) {
-      tc::tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col = 64 * tq + 32 * c;
-        float v[32];
-        tmem_ld32(tl + kColO + col, v);
-        const int j = col >> 6, g = 4 * r + j;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int cc = (col & 63) + e;
-          orow[g * 64 + tc::chan_of_pos(cc >> 3, cc & 7, kTypeB)] = v[e] + mt[j];
-        }
-      }
-      if (r == 0 && tq == 0) {
-        a.part_ml[((long long)sidx * a.H + h) * 2] = m_run;
-        a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = l_tot;
-      }
-    } else {
-      for (int c = 0; c < 64; ++c) orow[(4 * r + tq) * 64 + c] = 0.f;
-      if (r == 0 && tq == 0) {
-        a.part_ml[((long long)sidx * a.H + h) * 2] = -INFINITY;
-        a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = 0.f;
-      }
-    }
-  } else {
-    // ---------------- MMA issue (lane 0): QK of the next tile's first two
-    // groups, then PV of this tile, then the rest of the next tile's QK
+  } else if (warp == kIssuerWarp) {
+    // ---------------- MMA issue (lane 0): the next tile's QK as soon as its
+    // planes are in and the softmax warps have read this tile's logits; then
+    // this tile's PV once P is in tensor memory
     if (lane == 0) {
-      const uint32_t id_qk = tc::idesc(128, 64, 0, 0);  // A K-major, B K-major
-      const uint32_t id_pv = tc::idesc(128, 64, 0, 1);  // A (tensor memory), B MN-major
-      int kq = 0;
-      auto issue_qk = [&](int i, int j) -> bool {
-        const int slot = kq & 1;
-        if (kq >= 2 && !wait(bar(kBarDFree + slot), ((kq >> 1) - 1) & 1, abort_flag, a.err))
-          return false;
-        tc::tc_fence_after();
-        const uint32_t qa = tc::su32(sQ + j * kQBlock);
-        const uint32_t pb = tc::su32(sA + (i % kNB) * kMaxOwn * kPlane + j * kPlane);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma(tmem + kColD + 64 * slot, tc::desc(qa + 32 * ks, 16, 1024),
-                  tc::desc(pb + 32 * ks, 16, 1024), id_qk, ks > 0);
-        tc::commit(bar(kBarDFull + slot));
-        ++kq;
-        return true;
-      };
+      const uint32_t id_qk = tc::idesc(128, 64, 0, 0);    // A K-major, B K-major
+      const uint32_t id_pv = tc::idesc(128, 256, 0, 1);   // A (tensor memory), B MN-major
       auto tile_ready = [&](int i) {
         const bool r2 = wait(bar(kBarAFull + i % kNB), (i / kNB) & 1, abort_flag, a.err);
         if (r2) tc::tc_fence_after();
         return r2;
       };
-      bool ok = n_tiles > 0 && tile_ready(0);
-      for (int j = 0; ok && j < n_own; ++j) ok = issue_qk(0, j);
-      auto issue_pv = [&](int i, int j) -> bool {
-        const int kp = 4 * i + j, pslot = kp & 1;
-        if (!wait(bar(kBarPsFull + pslot), (kp >> 1) & 1, abort_flag, a.err)) return false;
-        tc::tc_fence_after();
-        const uint32_t pb = tc::su32(sA + (i % kNB) * kMaxOwn * kPlane + j * kPlane);
-        const uint32_t ps = tmem + kColPs + 64 * pslot;
+      // descriptors differ only in their start address (16-byte units in the
+      // low bits, no carry for shared-memory addresses)
+      const uint64_t kq0 = tc::desc(tc::su32(sA), 16, 1024);
+      const uint64_t kp0 = tc::desc(tc::su32(sA), kPlane, 1024);
+      const uint64_t qr0 = tc::desc(tc::su32(sQR), 16, 1024);
+      auto issue_qk = [&](int i) {
+        const uint64_t d = kq0 + (uint64_t)(((i % kNB) * kABuf) >> 4);
+        int acc = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t qa = tmem + kColQ + 32 * j + 8 * ks;
+            mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, acc);
+            mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
+            acc = 1;
+          }
+        }
+        // this rank's half of the RoPE channels: k-steps 2r, 2r + 1
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int ks = 2 * r + k2;
+          tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                  d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_qk, 1);
+          tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                  d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
+        }
+        tc::commit(bar(kBarDFull));
+      };
+      auto issue_pv = [&](int i) {
+        const uint64_t d = kp0 + (uint64_t)(((i % kNB) * kABuf) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = tc::desc(pb + 2048 * ks, 1024, 1024);
-          mma_tmem_a(tmem + kColO + 64 * j, ps + 8 * ks, bd, id_pv, (i > 0 || ks > 0));
-          mma_tmem_a(tmem + kColO + 64 * j, ps + 32 + 8 * ks, bd, id_pv, 1);
+          // the four content groups' planes side by side: N = 256 channels
+          const uint64_t b1 = d + (uint64_t)((2048 * ks) >> 4);
+          const uint64_t b2 = d + (uint64_t)((kMaxOwn * kPlane + 2048 * ks) >> 4);
+          const uint32_t phi = tmem + kColP + 8 * ks, plo = tmem + kColP + 32 + 8 * ks;
+          mma_tmem_a(tmem + kColO, phi, b1, id_pv, (i > 0 || ks > 0));
+          mma_tmem_a(tmem + kColO, plo, b1, id_pv, 1);
+          mma_tmem_a(tmem + kColO, phi, b2, id_pv, 1);
         }
-        tc::commit(bar(kBarPsFree + pslot));
-        return true;
-      };
-      // order per tile: the next tile's first two QK groups, PV of groups 0
-      // and 1, the rest of the next tile's QK (its slots are freed by the
-      // softmax warps' fold, which follows their P*s writes for this tile),
-      // then PV of groups 2 and 3
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const bool nxt = i + 1 < n_tiles;
-        if (nxt) {
-          ok = tile_ready(i + 1);
-          for (int j = 0; ok && j < 2; ++j) ok = issue_qk(i + 1, j);
-        }
-        for (int j = 0; ok && j < 2; ++j) ok = issue_pv(i, j);
-        for (int j = 2; ok && nxt && j < n_own; ++j) ok = issue_qk(i + 1, j);
-        for (int j = 2; ok && j < 4; ++j) ok = issue_pv(i, j);
-        if (!ok) break;
-        tc::commit(bar(kBarPV));
+        tc::commit(bar(kBarPFree));
         tc::commit(bar(kBarAFree + i % kNB));
+      };
+      bool ok = n_tiles > 0 && tile_ready(0);
+      if (ok) issue_qk(0);
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        if (i + 1 < n_tiles) {
+          ok = tile_ready(i + 1) && wait(bar(kBarDFree), i & 1, abort_flag, a.err);
+          if (!ok) break;
+          tc::tc_fence_after();
+          issue_qk(i + 1);
+        }
+        ok = wait(bar(kBarPFull), i & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc::tc_fence_after();
+        issue_pv(i);
       }
       // drain (bounded, regardless of the abort flag) before TMEM is freed
       tc::commit(bar(kBarFlush));
@@ -786,6 +701,203 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           set_error(a.err, MLA_LOWBIT_DEV_PIPELINE);
           break;
         }
+      }
+    }
+  } else if (warp >= kSoftWarp0) {
+    // ---------------- softmax: row h (TMEM lane), tokens kTW*th .. kTW*th+kTW-1
+    const int qd = warp & 3, th = (warp - kSoftWarp0) >> 2, h = 32 * qd + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+    const uint32_t x_peer = map_peer(tc::su32(sX), peer);
+    // warp w exchanges with the peer's warp w only (same rows, same tokens),
+    // through a pair of barriers of its own
+    const int sw_idx = warp - kSoftWarp0;
+    const uint32_t xfull_peer = map_peer(bar(kBarXFull + sw_idx), peer);
+    const uint32_t xfree_peer = map_peer(bar(kBarXFree + sw_idx), peer);
+    // rows of query block qb see all but the last n_q - 1 - qb protected tokens
+    const int n_masked = a.n_q - 1 - h / (kRows / a.n_q);
+    float m_run = -INFINITY, l = 0.f;
+    float accm[4] = {0.f, 0.f, 0.f, 0.f};
+    bool ok = true;
+    int done_tiles = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int buf = i % kNB;
+      const bool packed_tile = i < n_pk;
+      const float* meta = sMeta + buf * kMaxOwn * 64 + kTW * th;
+      const float4* f4 = reinterpret_cast<const float4*>(sShift + buf * 64 + kTW * th);
+      float S[kTW];
+      // partial logits of my groups: the accumulator (scaled back per token)
+      // plus the min terms.  The unpack warps' metadata of this tile is read
+      // after an acquire on its plane-ready barrier (complete by now: QK ran).
+      if (ok) ok = wait(bar(kBarDFull), i & 1, abort_flag, a.err);
+      if (ok) ok = wait(bar(kBarAFull + buf), (i / kNB) & 1, abort_flag, a.err);
+      const uint32_t vmask = sMask[buf * 4 + 2 * th] | (sMask[buf * 4 + 2 * th + 1] << 16);
+      ok = warp_all(ok);
+      if (ok) {
+        tc::tc_fence_after();
+        tmem_ld32(tl + kColD + kTW * th, S);
+        tc::tc_fence_before();
+        tc::bar_arrive(bar(kBarDFree));
+#pragma unroll
+        for (int t4 = 0; t4 < kTW / 4; ++t4) {
+          const float4 f = f4[t4];
+          S[4 * t4] *= f.x;
+          S[4 * t4 + 1] *= f.y;
+          S[4 * t4 + 2] *= f.z;
+          S[4 * t4 + 3] *= f.w;
+        }
+        // min terms: the content groups, and (rank 1) the RoPE group
+#pragma unroll
+        for (int j = 0; j < kMaxOwn; ++j) {
+          if (j >= n_own) break;
+          const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64);
+#pragma unroll
+          for (int t4 = 0; t4 < kTW / 4; ++t4) {
+            const float4 mv = m4[t4];
+            S[4 * t4] = fmaf(mv.x, qs[j], S[4 * t4]);
+            S[4 * t4 + 1] = fmaf(mv.y, qs[j], S[4 * t4 + 1]);
+            S[4 * t4 + 2] = fmaf(mv.z, qs[j], S[4 * t4 + 2]);
+            S[4 * t4 + 3] = fmaf(mv.w, qs[j], S[4 * t4 + 3]);
+          }
+        }
+      }
+      // exchange with the peer: my partial of my kTW tokens goes to the
+      // peer's buffer (once the peer has read the previous tile's), the peer's
+      // partial of the same tokens arrives in mine
+      if (ok && i >= 1) ok = bar_wait_cluster(bar(kBarXFree + sw_idx), (i - 1) & 1, abort_flag, a.err);
+      if (ok) {
+        const uint32_t dst = x_peer + (uint32_t)((th * kRows + h) * kXStride) * 4u;
+#pragma unroll
+        for (int k = 0; k < kTW / 4; ++k)
+          st_async4(dst + 16 * k, S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3], xfull_peer);
+        if (lane == 0) expect_tx(bar(kBarXFull + sw_idx), 32 * kTW * 4);
+        ok = wait(bar(kBarXFull + sw_idx), i & 1, abort_flag, a.err);
+      }
+      if (ok) {
+        const float4* src = reinterpret_cast<const float4*>(sX + (th * kRows + h) * kXStride);
+#pragma unroll
+        for (int k = 0; k < kTW / 4; ++k) {
+          const float4 v = src[k];
+          S[4 * k] += v.x;
+          S[4 * k + 1] += v.y;
+          S[4 * k + 2] += v.z;
+          S[4 * k + 3] += v.w;
+        }
+      }
+      // validity, log2 scale, tile max over both halves
+      const int tok0 = bf_first + (i - n_pk) * 64 + kTW * th;  // bf16 tiles
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kTW; ++t) {
+        const bool v = packed_tile ? ((vmask >> t) & 1u) != 0
+                                   : (tok0 + t < bf_end && tok0 + t < sw.n_tok - n_masked);
+        S[t] = v ? S[t] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, S[t]);
+      }
+      sMax[((i & 1) * 2 + th) * kRows + h] = mx;
+      if (pair_any(!ok, qd)) break;  // both warps of the rows leave at the same tile
+      // my reads of the peer's partial are done: one arrival per warp, issued
+      // after the tile max so that it does not queue ahead of local accesses
+      __syncwarp();
+      if (lane == 0) arrive_peer_relaxed(xfree_peer);
+      const float tmax = fmaxf(sMax[((i & 1) * 2) * kRows + h], sMax[((i & 1) * 2 + 1) * kRows + h]);
+      // lazy running max: moved only when the tile max exceeds it by kLazy
+      const bool need = m_run != -INFINITY && tmax > m_run + kLazy;
+      const float m_new = (m_run == -INFINITY || need) ? tmax : m_run;
+      // the previous tile's PV must be complete: P is reused, and O may be rescaled
+      if (ok && i >= 1) ok = wait(bar(kBarPFree), (i - 1) & 1, abort_flag, a.err);
+      ok = warp_all(ok);
+      if (ok && __any_sync(0xffffffffu, need)) {
+        tc::tc_fence_after();
+        const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
+        l *= alpha;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) accm[j] *= alpha;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t col = kColO + 128 * th + 32 * c;
+          float v[32];
+          tmem_ld32(tl + col, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= alpha;
+          tmem_st32(tl + col, v);
+        }
+      }
+      m_run = m_new;
+      float lsum = 0.f;
+#pragma unroll
+      for (int t = 0; t < kTW; ++t) {
+        S[t] = S[t] == -INFINITY ? 0.f : fast_exp2(S[t] - m_run);
+        lsum += S[t];
+      }
+      l += lsum;
+      // min terms of my four PV groups (unscaled P)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64);
+        float am = 0.f;
+#pragma unroll
+        for (int t4 = 0; t4 < kTW / 4; ++t4) {
+          const float4 mv = m4[t4];
+          am = fmaf(S[4 * t4], mv.x, am);
+          am = fmaf(S[4 * t4 + 1], mv.y, am);
+          am = fmaf(S[4 * t4 + 2], mv.z, am);
+          am = fmaf(S[4 * t4 + 3], mv.w, am);
+        }
+        accm[j] += am;
+      }
+      // P (times each token's plane factor) as fp16 high and low parts
+      if (ok) {
+        tc::tc_fence_after();
+        uint32_t hi[kTW / 2], lo[kTW / 2];
+#pragma unroll
+        for (int t4 = 0; t4 < kTW / 4; ++t4) {
+          const float4 f = f4[t4];
+          split_trunc(S[4 * t4] * f.x, S[4 * t4 + 1] * f.y, hi[2 * t4], lo[2 * t4]);
+          split_trunc(S[4 * t4 + 2] * f.z, S[4 * t4 + 3] * f.w, hi[2 * t4 + 1], lo[2 * t4 + 1]);
+        }
+        tmem_st16_nowait(tl + kColP + (kTW / 2) * th, hi);
+        tmem_st16_nowait(tl + kColP + 32 + (kTW / 2) * th, lo);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc::tc_fence_before();
+        tc::bar_arrive(bar(kBarPFull));
+      }
+      done_tiles = i + 1;
+    }
+    // ---- epilogue: the halves' l and min terms through the exchange buffer
+    // (no more traffic from the peer), then my 128 output columns (groups 2th, 2th+1)
+    soft_sync();
+    bool done = ok && n_tiles > 0 && done_tiles == n_tiles &&
+                wait(bar(kBarPFree), (n_tiles - 1) & 1, abort_flag, a.err);
+    done = !soft_any(!done);  // one decision for all softmax warps
+    sX[(th * 5) * kRows + h] = l;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sX[(th * 5 + 1 + j) * kRows + h] = accm[j];
+    soft_sync();
+    const float l_tot = sX[h] + sX[5 * kRows + h];
+    float* orow = a.part_o + ((long long)sidx * a.H + h) * kLatent;
+    if (done) {
+      tc::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int j = 2 * th + (c >> 1), g = 4 * r + j;
+        const float mt = sX[(1 + j) * kRows + h] + sX[(6 + j) * kRows + h];
+        float v[32];
+        tmem_ld32(tl + kColO + 128 * th + 32 * c, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int cc = 32 * (c & 1) + e;
+          orow[g * 64 + tc::chan_of_pos(cc >> 3, cc & 7, kTypeB)] = v[e] + mt;
+        }
+      }
+      if (r == 0 && th == 0) {
+        a.part_ml[((long long)sidx * a.H + h) * 2] = m_run;
+        a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = l_tot;
+      }
+    } else {
+      for (int c = 0; c < 128; ++c) orow[(4 * r + 2 * th) * 64 + c] = 0.f;
+      if (r == 0 && th == 0) {
+        a.part_ml[((long long)sidx * a.H + h) * 2] = -INFINITY;
+        a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = 0.f;
       }
     }
   }
