@@ -24,8 +24,10 @@
 //   logit and P scaled back by 2^4 (exact powers of two).
 // * q of the content groups lives in tensor memory and is the A operand of
 //   QK; the partial logits cross the cluster with st.async into the peer's
-//   shared memory (the sum is commutative, so both CTAs hold bit-identical
-//   logits and make the same online-softmax decisions); P is written by the
+//   shared memory, each softmax warp with the peer's warp of the same rows
+//   and tokens through a barrier pair of its own (the sum is commutative, so
+//   both CTAs hold bit-identical logits and make the same online-softmax
+//   decisions); P is written by the
 //   softmax warps straight into tensor memory as the A operand of PV; O
 //   (128 x 256 fp32) stays in tensor memory for the whole split and is
 //   rescaled only when a row's running max grows by more than kLazy.

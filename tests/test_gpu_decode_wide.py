@@ -131,3 +131,43 @@ def test_wide_large_scales_under_the_lazy_max():
     assert np.all(np.isfinite(got))
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel <= 1e-3 and np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max(), (rel, np.abs(got - ref).max())
+
+
+def test_wide_scales_beyond_the_fp16_plane_range():
+    # Content groups spanning +-31000: the fp16 scale is ~4100, so s * |c - 8|
+    # reaches ~33000 and the kernel stores those tokens' planes scaled by 2^-4
+    # (and scales their logits and P back).  Relative bar, as the outputs are
+    # O(1e4): rel-L2 <= 1e-3 and max-abs <= 1e-3 of the largest value (fp32
+    # tensor-core accumulation over 1,500 products of this size carries ~1e-4
+    # relative error; a wrong compensation would be off by a factor of 16).
+    import torch
+    import bit_mla_kv_lowbit_gb300 as pkg
+    rng = np.random.default_rng(92)
+    L, H = 1500, 128
+    ckv = rng.uniform(-31000.0, 31000.0, (L, 512))
+    ckv[::3, 64:128] *= 1e-3          # some groups on every third token stay small
+    kr = rng.standard_normal((L, 64))
+    q = rng.standard_normal((H, 576)) * 1e-4
+    to_bits = lambda x: syn.bf16_bits_from_f32(np.asarray(x, dtype=np.float32))
+    ckv_b, kr_b, q_b = to_bits(ckv), to_bits(kr), to_bits(q)
+    table = np.arange(24, dtype=np.int32)[None, :]
+    cache = pkg.PagedCache(4, 4, table, 24, "cuda")
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    cache.write(to_dev(ckv_b, torch.bfloat16), to_dev(kr_b, torch.bfloat16),
+                torch.arange(L, dtype=torch.int32, device="cuda"),
+                seq_idx=torch.zeros(L, dtype=torch.int32, device="cuda"), seq_lens_after=lens)
+    scale = 1.0 / np.sqrt(192.0)
+    lse = torch.empty(1, H, dtype=torch.float32, device="cuda")
+    out = cache.decode(to_dev(q_b[None], torch.bfloat16), lens, [L], scale, lse=lse)
+    torch.cuda.synchronize()
+    assert cache.error() == 0
+    got = out.cpu().numpy()[0].astype(np.float64)
+    model = oracle.PagedCacheModel(oracle.Layout(4, 4), 24, table)
+    model.write(np.zeros(L, np.int64), np.arange(L), ckv_b, kr_b, np.array([L]))
+    ref, ref_lse = oracle.mla_decode_fp64(q_b, model.effective_keys(0, L), scale)
+    assert np.all(np.isfinite(got))
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= 1e-3 and np.abs(got - ref).max() <= 1e-3 * np.abs(ref).max(), (rel, np.abs(got - ref).max())
+    # each logit sums 576 products of size ~3 here: fp32 accumulation alone
+    # leaves ~1e-4 in the log-sum-exp, hence a 1e-3 bar instead of 1e-4
+    assert np.allclose(lse.cpu().numpy()[0], ref_lse, rtol=0, atol=1e-3)
