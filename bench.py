@@ -543,18 +543,20 @@ def run_table9(args):
 
 
 def run_mtp(args):
-    """Multi-token query decode on the v2lite shape (B8 H16 L32768 C4R4): decode
-    time for 1, 2, 4 and 8 causal queries per sequence over the same cache (the
-    Group-Query Latent Attention abstract's s_q = 2 multi-token prediction
-    step; 8 queries of 16 heads are 128 rows, which the 2-CTA tcgen05 kernel
-    takes). One JSON line per query count; L2 flushed before each timed call."""
+    """Multi-token query decode: decode time for several causal queries per
+    sequence over the same cache (the Group-Query Latent Attention abstract's
+    s_q = 2 multi-token prediction step).  On the v2lite shape (B8 H16 L32768
+    C4R4) 1, 2, 4 and 8 queries (8 queries of 16 heads are 128 rows, which the
+    2-CTA tcgen05 kernel takes); on a 128-head shape (--sweep-workload v3_c4r4)
+    1 and 2 queries (128 and 256 rows).  One JSON line per query count; L2
+    flushed before each timed call."""
     import torch
-    w = syn.get("v2lite_c4r4")
+    w = syn.get(args.sweep_workload)
     s = Setup(w, "cuda:0")
     peak, peak_kind = peaks()
     tpk, tpk_kind = tensor_peak()
     base = None
-    for n in (1, 2, 4, 8):
+    for n in ((1, 2, 4, 8) if w.heads <= 16 else (1, 2)):
         g = torch.Generator(device="cuda")
         g.manual_seed(100 + n)
         q = torch.randn(w.batch, n, w.heads, 576, generator=g, device="cuda").to(torch.bfloat16)
@@ -635,6 +637,8 @@ def main():
                     help="context-length sweep, multi-token query decode or the cost of the "
                          "online rotation, instead of the benchmark line")
     ap.add_argument("--sweep-heads", type=int, default=16)
+    ap.add_argument("--sweep-workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS),
+                    help="workload of the multi-query sweep")
     ap.add_argument("--sweep-reps", type=int, default=15)
     args = ap.parse_args()
     if args.sweep == "table9":

@@ -177,8 +177,9 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
 // True when launch_decode can append each sequence's new token itself (the
 // DecodeArgs new_* fields): the default split kernel on a packed layout.
 bool decode_fuses_append(int cbits, int rotate, int rows);
-// CTAs that process one split (head chunks of 16, or the 2-CTA cluster of the
-// 128-row tcgen05 kernel): the planner sizes chunks so that all fit one wave.
+// CTAs that process one split (head chunks of 16, or one 2-CTA cluster per
+// 128-row block for the tcgen05 kernel): the planner sizes chunks so that all
+// fit one wave.
 int decode_ctas_per_split(int cbits, int rows, int rotate);
 cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_hy(int cbits, const DecodeArgs& a, cudaStream_t stream);

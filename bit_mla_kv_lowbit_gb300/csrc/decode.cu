@@ -737,9 +737,10 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, combine_kernel, ca);
 }
 
-// Kernel for a layout and a row count (n_q * heads): packed caches with
-// exactly 128 rows and no rotation take the 2-CTA tcgen05 kernel
-// (decode_wide.cu); everything else the mma.sync kernel above (the fastest
+// Kernel for a layout and a row count (n_q * heads): packed caches with a
+// multiple of 128 rows and no rotation take the 2-CTA tcgen05 kernel
+// (decode_wide.cu, one cluster per split and 128-row block); everything else
+// the mma.sync kernel above (the fastest
 // measured on GB300 for 16-head chunks).  MLA_LOWBIT_DECODE overrides the
 // choice: "m" always the mma.sync kernel; for packed single-query
 // unrotated decodes "h" the hybrid mma.sync + tcgen05 kernel (decode_hy.cu),
@@ -749,7 +750,7 @@ enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp, kWide };
 static SplitKernel split_kernel(int cbits, int n_q, int rotate, int rows) {
   const char* v = getenv("MLA_LOWBIT_DECODE");
   const char k = v ? v[0] : 0;
-  if (k == 0 && cbits != 16 && !rotate && rows == 128) return SplitKernel::kWide;
+  if (k == 0 && cbits != 16 && !rotate && rows % 128 == 0) return SplitKernel::kWide;
   // the only one with query blocks and with rotated queries
   if (cbits == 16 || n_q > 1 || rotate) return SplitKernel::kMma;
   if (k == 'h') return SplitKernel::kHybrid;
@@ -759,7 +760,7 @@ static SplitKernel split_kernel(int cbits, int n_q, int rotate, int rows) {
 }
 
 int decode_ctas_per_split(int cbits, int rows, int rotate) {
-  return split_kernel(cbits, 1, rotate, rows) == SplitKernel::kWide ? 2 : rows / kHC;
+  return split_kernel(cbits, 1, rotate, rows) == SplitKernel::kWide ? 2 * (rows / 128) : rows / kHC;
 }
 
 bool decode_fuses_append(int cbits, int rotate, int rows) {

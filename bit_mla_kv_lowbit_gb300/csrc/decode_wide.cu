@@ -1,6 +1,7 @@
-// Split-KV low-bit MLA decode for 128 query rows per sequence (128 heads, or
-// n_q query blocks of 128 / n_q heads) on the 5th-generation tensor cores, one
-// 2-CTA cluster per split, for packed caches.
+// Split-KV low-bit MLA decode for query rows in blocks of 128 per sequence
+// (128 heads, n_q query blocks of 128 / n_q heads, or n_q blocks of 128 heads)
+// on the 5th-generation tensor cores, one 2-CTA cluster per (split, 128-row
+// block), for packed caches.
 //
 // Same arithmetic as decode.cu (QuantMLA, Abstract and Figure 8 caption:
 // exact integer codes on the tensor cores, per-group fp16 scale and min, one
@@ -311,6 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int r = (int)cluster_rank();
   const uint32_t peer = r ^ 1;
   const int sidx = blockIdx.x >> 1;  // the split's global index
+  const int hb = kRows * blockIdx.y;  // first query row of this cluster
 
   int b, split, nsplit;
   find_split<kThreads>(a, true, scan, b, split, nsplit, sidx);
@@ -319,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int v = a.seq_lens[b];
     return (v < 0 || v > a.max_pages * kPageTokens) ? 0 : v;
   }();
-  if (split == 0 && r == 0 && tid == 0) {
+  if (split == 0 && r == 0 && blockIdx.y == 0 && tid == 0) {
     a.seq_split[2 * b] = sidx;
     a.seq_split[2 * b + 1] = nsplit;
   }
@@ -362,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   {
     for (int u = tid; u < kRows * 4; u += kThreads) {
       const int h = u >> 2, cc = u & 3;
-      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((long long)b * a.H + h) * kDim + 512 + 16 * cc);
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((long long)b * a.H + hb + h) * kDim + 512 + 16 * cc);
       const uint4 v0 = src[0], v1 = src[1];
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
@@ -392,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   float qs[kMaxOwn] = {0.f, 0.f, 0.f, 0.f, 0.f};
   if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 8) {
     const int qd = warp & 3, th = (warp - kSoftWarp0) >> 2, h = 32 * qd + lane;
-    const uint16_t* qrow = a.q + ((long long)b * a.H + h) * kDim;
+    const uint16_t* qrow = a.q + ((long long)b * a.H + hb + h) * kDim;
 #pragma unroll
     for (int j = 0; j < kMaxOwn; ++j) {
       const int g = j < 4 ? 4 * r + j : 8;
@@ -716,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t xfull_peer = map_peer(bar(kBarXFull + sw_idx), peer);
     const uint32_t xfree_peer = map_peer(bar(kBarXFree + sw_idx), peer);
     // rows of query block qb see all but the last n_q - 1 - qb protected tokens
-    const int n_masked = a.n_q - 1 - h / (kRows / a.n_q);
+    const int n_masked = a.n_q - 1 - (hb + h) / (a.H / a.n_q);
     float m_run = -INFINITY, l = 0.f;
     float accm[4] = {0.f, 0.f, 0.f, 0.f};
     bool ok = true;
@@ -876,7 +878,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 4; ++j) sX[(th * 5 + 1 + j) * kRows + h] = accm[j];
     soft_sync();
     const float l_tot = sX[h] + sX[5 * kRows + h];
-    float* orow = a.part_o + ((long long)sidx * a.H + h) * kLatent;
+    float* orow = a.part_o + ((long long)sidx * a.H + hb + h) * kLatent;
     if (done) {
       tc::tc_fence_after();
 #pragma unroll 1
@@ -892,14 +894,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (r == 0 && th == 0) {
-        a.part_ml[((long long)sidx * a.H + h) * 2] = m_run;
-        a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = l_tot;
+        a.part_ml[((long long)sidx * a.H + hb + h) * 2] = m_run;
+        a.part_ml[((long long)sidx * a.H + hb + h) * 2 + 1] = l_tot;
       }
     } else {
       for (int c = 0; c < 128; ++c) orow[(4 * r + 2 * th) * 64 + c] = 0.f;
       if (r == 0 && th == 0) {
-        a.part_ml[((long long)sidx * a.H + h) * 2] = -INFINITY;
-        a.part_ml[((long long)sidx * a.H + h) * 2 + 1] = 0.f;
+        a.part_ml[((long long)sidx * a.H + hb + h) * 2] = -INFINITY;
+        a.part_ml[((long long)sidx * a.H + hb + h) * 2 + 1] = 0.f;
       }
     }
   }
@@ -930,7 +932,7 @@ cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stre
     if (e != cudaSuccess) return e;
     configured[k] = true;
   }
-  dim3 grid(2 * a.total_splits), block(wide::kThreads);
+  dim3 grid(2 * a.total_splits, a.H / wide::kRows), block(wide::kThreads);
   if (cbits == 4)
     wide::decode_wide_kernel<4><<<grid, block, smem, stream>>>(a);
   else

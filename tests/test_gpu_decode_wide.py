@@ -171,3 +171,33 @@ def test_wide_scales_beyond_the_fp16_plane_range():
     # each logit sums 576 products of size ~3 here: fp32 accumulation alone
     # leaves ~1e-4 in the log-sum-exp, hence a 1e-3 bar instead of 1e-4
     assert np.allclose(lse.cpu().numpy()[0], ref_lse, rtol=0, atol=1e-3)
+
+
+@pytest.mark.parametrize("cb", [4, 2])
+def test_wide_two_row_blocks_mtp_128_heads(cb):
+    # 2 causal queries of 128 heads (256 rows: two 128-row clusters per split),
+    # the multi-token prediction step of a 128-head model
+    import torch
+    heads, n = 128, 2
+    w = syn.custom(f"wide_mtp128_c{cb}", [6, 133, 700, 3100], heads=heads, content_bits=cb,
+                   steps=n, seed=95)
+    run = GpuRun(w)
+    run.prefill()
+    ckv, kr, _ = run.step_inputs(0)
+    lens = run.lens.astype(np.int32)
+    run.cache.write(to_dev(ckv, torch.bfloat16), to_dev(kr, torch.bfloat16),
+                    to_dev(lens - 1, torch.int32), seq_lens_after=to_dev(lens, torch.int32))
+    q = np.stack([syn.queries(w, b)[:n] for b in range(w.batch)])
+    lse = torch.empty(w.batch, n, heads, dtype=torch.float32, device="cuda")
+    out = run.cache.decode_multi(to_dev(q, torch.bfloat16), to_dev(lens, torch.int32),
+                                 [int(x) for x in lens], w.softmax_scale, lse=lse)
+    torch.cuda.synchronize()
+    assert run.cache.error() == 0
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    for b in range(w.batch):
+        model, L = oracle_model(run, b, 0)
+        ref, ref_lse = oracle.mla_decode_multi_fp64(q[b], model.effective_keys(b, L),
+                                                    w.softmax_scale)
+        for i in range(n):
+            check_attention(out[b, i], ref[i], f"seq {b} (L={L}) query {i}")
+            assert np.allclose(lse[b, i], ref_lse[i], rtol=0, atol=1e-4), f"lse seq {b} query {i}"
