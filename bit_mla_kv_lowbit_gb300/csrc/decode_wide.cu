@@ -20,7 +20,9 @@
 //   and PV runs with one operand P for all groups of the CTA (N = 256):
 //   O += P_hi (s_hi c) + P_lo (s_hi c) + P_hi (s_lo c), with P split into fp16
 //   high and low parts once per row and token.  The min terms (m' = m + centre
-//   s) are rank-one sums done in fp32 on the CUDA cores.  A token whose scale
+//   s) of the logits run on the tensor core too, as two bf16 k-steps of QK
+//   (factors split in three bf16 parts); those of the output are rank-one
+//   sums done in fp32 on the CUDA cores.  A token whose scale
 //   would take s c past the fp16 range has both planes scaled by 2^-4 and its
 //   logit and P scaled back by 2^4 (exact powers of two).
 // * q of the content groups lives in tensor memory and is the A operand of
@@ -67,9 +69,10 @@ constexpr float kShiftAbove = 32768.f;  // |s c| bound beyond which a token's pl
 // shared memory (bytes, from a 1 KB aligned base)
 constexpr int kOffA = 0;                                     // [kNB] plane sets
 constexpr int kOffQR = kOffA + kNB * kABuf;                  // RoPE q block
-constexpr int kXStride = 36;                                 // floats per exchange row (padded)
-constexpr int kOffX = kOffQR + kQBlock;                      // [2 halves][128 rows][kXStride] fp32
-constexpr int kOffMeta = kOffX + 2 * kRows * kXStride * 4;   // [kNB][5][64] fp32 m'
+// exchange buffer: [2 token halves][8 chunks of 4 tokens][128 rows] float4, so
+// that a warp's 16-byte stores (and loads) of one chunk are 512 contiguous bytes
+constexpr int kOffX = kOffQR + kQBlock;
+constexpr int kOffMeta = kOffX + 2 * 8 * kRows * 16;         // [kNB][5][64] fp32 m'
 constexpr int kOffShift = kOffMeta + kNB * kMaxOwn * 64 * 4; // [kNB][64] fp32 token factor
 constexpr int kOffValid = kOffShift + kNB * 64 * 4;          // [kNB][4] 16-token masks
 constexpr int kOffMax = kOffValid + kNB * 4 * 4;             // [2][2][128] fp32
@@ -224,6 +227,20 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int
   }
 }
 
+// v[t] *= f[t] for the 32 tokens of a softmax warp's half tile (the factor 16
+// of tokens whose planes were stored scaled by 2^-4); called only for tiles
+// that hold such a token.
+__device__ __forceinline__ void scale_by_token(float (&v)[kTW], const float4* f4) {
+#pragma unroll
+  for (int t4 = 0; t4 < kTW / 4; ++t4) {
+    const float4 f = f4[t4];
+    v[4 * t4] *= f.x;
+    v[4 * t4 + 1] *= f.y;
+    v[4 * t4 + 2] *= f.z;
+    v[4 * t4 + 3] *= f.w;
+  }
+}
+
 // OR of `pred` over the 256 softmax threads (named barrier 1).
 __device__ __forceinline__ bool soft_any(bool pred) {
   uint32_t r;
@@ -274,6 +291,57 @@ __device__ __forceinline__ void scale_parts(uint32_t s16, bool shift, uint32_t& 
   }
   hi2 = (uint32_t)__half_as_ushort(h2) * 0x00010001u;
   lo2 = (uint32_t)__half_as_ushort(lo) * 0x00010001u;
+}
+
+// Min terms on the tensor core.  The logit's min terms sum_j qs_j m'_j over
+// the CTA's groups (qs_j: the row's q summed over group j; m'_j: the token's
+// dequantised value at code 0 of group j) run as two bf16 k-steps of QK, in
+// the RoPE k-steps this rank leaves unused (both in the RoPE q block and in
+// the RoPE s_hi plane).  Each factor is split in three bf16 parts (h + m + l,
+// 24 significant bits; bf16 has the fp32 exponent range), and the two
+// k-steps carry the six products hh, hm, mh, hl, lh, mm of the five groups:
+//   k-step X  A: qh0-4 qh0-4 qm0-4 0    B: mh0-4 mm0-4 mh0-4 0
+//   k-step Y  A: qh0-4 ql0-4 qm0-4 0    B: ml0-4 mh0-4 mm0-4 0
+__device__ __forceinline__ float bf16_round(float x) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(0.f), "f"(x));
+  return __uint_as_float(d << 16);
+}
+__device__ __forceinline__ void split3_bf16(float x, float& h, float& m, float& l) {
+  h = bf16_round(x);
+  const float r1 = x - h;  // exact
+  m = bf16_round(r1);
+  l = bf16_round(r1 - m);  // r1 - m exact
+}
+// two floats that are bf16 values -> one bf16x2 word (lo in the low half)
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  return (__float_as_uint(hi) & 0xFFFF0000u) | (__float_as_uint(lo) >> 16);
+}
+// The 16-byte chunks of k-step X (c = 0, 1) and Y (c = 2, 3) for a row of
+// the RoPE q block (x = q parts) or a token of the plane (x = m' parts).
+__device__ __forceinline__ uint4 min_chunk_a(int c, const float* h, const float* m, const float* l) {
+  switch (c) {
+    case 0: return make_uint4(bf16x2_bits(h[0], h[1]), bf16x2_bits(h[2], h[3]), bf16x2_bits(h[4], h[0]),
+                              bf16x2_bits(h[1], h[2]));
+    case 1: return make_uint4(bf16x2_bits(h[3], h[4]), bf16x2_bits(m[0], m[1]), bf16x2_bits(m[2], m[3]),
+                              bf16x2_bits(m[4], 0.f));
+    case 2: return make_uint4(bf16x2_bits(h[0], h[1]), bf16x2_bits(h[2], h[3]), bf16x2_bits(h[4], l[0]),
+                              bf16x2_bits(l[1], l[2]));
+    default: return make_uint4(bf16x2_bits(l[3], l[4]), bf16x2_bits(m[0], m[1]), bf16x2_bits(m[2], m[3]),
+                               bf16x2_bits(m[4], 0.f));
+  }
+}
+__device__ __forceinline__ uint4 min_chunk_b(int c, const float* h, const float* m, const float* l) {
+  switch (c) {
+    case 0: return make_uint4(bf16x2_bits(h[0], h[1]), bf16x2_bits(h[2], h[3]), bf16x2_bits(h[4], m[0]),
+                              bf16x2_bits(m[1], m[2]));
+    case 1: return make_uint4(bf16x2_bits(m[3], m[4]), bf16x2_bits(h[0], h[1]), bf16x2_bits(h[2], h[3]),
+                              bf16x2_bits(h[4], 0.f));
+    case 2: return make_uint4(bf16x2_bits(l[0], l[1]), bf16x2_bits(l[2], l[3]), bf16x2_bits(l[4], h[0]),
+                              bf16x2_bits(h[1], h[2]));
+    default: return make_uint4(bf16x2_bits(h[3], h[4]), bf16x2_bits(m[0], m[1]), bf16x2_bits(m[2], m[3]),
+                               bf16x2_bits(m[4], 0.f));
+  }
 }
 
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
@@ -330,7 +398,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int bf_first = 64 * sw.bf_begin;
   const int bf_end = min(sw.n_tok, 64 * (sw.bf_begin + sw.n_bf));
   const int n_tiles = n_pk + max(0, (bf_end - bf_first + 63) / 64);
-  const int n_own = 4 + r;
 
   // ---- set-up: barriers, TMEM, page ids, RoPE q block
   if (tid == 0) {
@@ -418,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&o[p2]));
         acc += hf.x + hf.y;
       }
-      qs[j] = acc;
+      qs[j] = j < 4 || r == 1 ? acc : 0.f;  // the RoPE group's min term is rank 1's
       if (j < 4 && (j >> 1) == th) {
         const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
         tmem_st8_nowait(tl + kColQ + 32 * j, o);
@@ -427,6 +494,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st8_nowait(tl + kColQ + 32 * j + 24, o + 24);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
+    }
+    if (th == 0) {
+      float qh[kMaxOwn], qm[kMaxOwn], ql[kMaxOwn];
+#pragma unroll
+      for (int j = 0; j < kMaxOwn; ++j) split3_bf16(qs[j], qh[j], qm[j], ql[j]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(sQR + tc::sw_chunk(h, 4 * (1 - r) + c)) = min_chunk_a(c, qh, qm, ql);
+      tc::fence_async_smem();
     }
   }
   tc::tc_fence_before();
@@ -476,13 +552,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) cc[k] = nc[k];
       const uint2 rr = nr;
-      const uint32_t mw[3] = {nm[0], nm[1], nm[2]};
+      uint32_t mw[3] = {nm[0], nm[1], nm[2]};
       const bool okt_cur = n_okt;
       if (i + 1 < n_pk) fetch(i + 1);  // in flight while the buffer drains
       if (i >= kNB && !wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err)) break;
       uint8_t* A = sA + buf * kABuf;
       float* meta = sMeta + buf * kMaxOwn * 64;
-      bool okt;
+      bool okt, shifted = false;
       if (i < n_pk) {
         okt = okt_cur;
         // one factor per token: 2^-4 on both planes when some group's s * |c|
@@ -495,19 +571,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
         const bool shift = smax > kShiftAbove;
+        shifted = shift;
         if (gh == 0) sShift[buf * 64 + t] = shift ? 16.f : 1.f;
-#pragma unroll
+        // the thread's two content groups in a rolled loop (code size): the
+        // group in hand is always cc[0..], mw[0], shifted down afterwards
+        float mq0 = 0.f, mq1 = 0.f;  // m' of the two groups, in order
+#pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * gh + jj;
           uint32_t hi2, lo2;
-          scale_parts(mw[jj] & 0xFFFFu, shift, hi2, lo2);
+          scale_parts(mw[0] & 0xFFFFu, shift, hi2, lo2);
           uint8_t* p1 = A + j * kPlane;
           uint8_t* p2 = A + (kMaxOwn + j) * kPlane;
           // the token's two threads write the same positions of planes 8 KB
           // apart (same banks): the second one walks the chunks in another
           // order, so that their stores never meet in one bank
           if constexpr (CB == 4) {
-            const uint4 c0 = cc[2 * jj], c1 = cc[2 * jj + 1];
+            const uint4 c0 = cc[0], c1 = cc[1];
             const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
             for (int k2 = 0; k2 < 8; ++k2) {
@@ -520,7 +600,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   make_uint4(hmul2u(p[0], lo2), hmul2u(p[1], lo2), hmul2u(p[2], lo2), hmul2u(p[3], lo2));
             }
           } else {
-            const uint4 c0 = cc[jj];
+            const uint4 c0 = cc[0];
             const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
@@ -538,8 +618,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
           }
-          const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw[jj]));
-          meta[j * 64 + t] = fmaf(kCentreC, sm.x, sm.y);
+          const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw[0]));
+          const float mq = fmaf(kCentreC, sm.x, sm.y);
+          meta[j * 64 + t] = mq;
+          mq0 = mq1;
+          mq1 = mq;
+          if constexpr (CB == 4) {
+            cc[0] = cc[2];
+            cc[1] = cc[3];
+          } else {
+            cc[0] = cc[1];
+          }
+          mw[0] = mw[1];
         }
         {
           // RoPE words 4r + 2gh, 4r + 2gh + 1 -> chunks of the same index
@@ -558,10 +648,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, c)) =
                 make_uint4(hmul2u(p[0], lo2), hmul2u(p[1], lo2), hmul2u(p[2], lo2), hmul2u(p[3], lo2));
           }
-          if (gh == 0) {
-            const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw[2]));
-            meta[4 * 64 + t] = fmaf(float(kCentre4), sm.x, sm.y);
-          }
+        }
+        {
+          // min-term k-steps of the token (B side): m' of the CTA's content
+          // groups (two from each thread of the token) and, on rank 1, of the
+          // RoPE group, times the token's plane factor; thread gh writes the
+          // chunks of k-step X (gh = 0) or Y (gh = 1)
+          const float2 smr = __half22float2(*reinterpret_cast<const __half2*>(&mw[2]));
+          const float pa = __shfl_xor_sync(0xffffffffu, mq0, 1);
+          const float pb = __shfl_xor_sync(0xffffffffu, mq1, 1);
+          const float f = shift ? 0.0625f : 1.f;
+          const float mv[kMaxOwn] = {gh ? pa : mq0, gh ? pb : mq1, gh ? mq0 : pa, gh ? mq1 : pb,
+                                     r ? fmaf(float(kCentre4), smr.x, smr.y) : 0.f};
+          float mh[kMaxOwn], mm[kMaxOwn], ml[kMaxOwn];
+#pragma unroll
+          for (int j = 0; j < kMaxOwn; ++j) split3_bf16(mv[j] * f, mh[j], mm[j], ml[j]);
+          uint8_t* p1 = A + 4 * kPlane;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
+            *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
+                min_chunk_b(2 * gh + c2, mh, mm, ml);
         }
       } else {
         // protected tokens: bf16 values as the s_hi plane, zero s_lo plane, min 0
@@ -607,15 +713,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         meta[(2 * gh) * 64 + t] = 0.f;
         meta[(2 * gh + 1) * 64 + t] = 0.f;
-        if (gh == 0) meta[4 * 64 + t] = 0.f;
+        // no min terms: zero min-term k-steps
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2)
+          *reinterpret_cast<uint4*>(A + 4 * kPlane + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
+              make_uint4(0, 0, 0, 0);
       }
-      // validity of the warp's 16 tokens (lanes 2k and 2k+1 hold token k)
+      // validity of the warp's 16 tokens (lanes 2k and 2k+1 hold token k);
+      // bit 31: some token of the 16 has its planes scaled by 2^-4
+      const bool any_shift = __any_sync(0xffffffffu, shifted);
       uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
       mk = (mk | (mk >> 1)) & 0x33333333u;
       mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
       mk = (mk | (mk >> 4)) & 0x00FF00FFu;
       mk = (mk | (mk >> 8)) & 0x0000FFFFu;
-      if (lane == 0) sMask[buf * 4 + warp] = mk;
+      if (lane == 0) sMask[buf * 4 + warp] = mk | (any_shift ? 0x80000000u : 0u);
       tc::fence_async_smem();
       tc::bar_arrive(bar(kBarAFull + buf));
     }
@@ -625,6 +737,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // this tile's PV once P is in tensor memory
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc(128, 64, 0, 0);    // A K-major, B K-major
+      // the same shape with bf16 A and B (bits 7-9, 10-12: format 1) for the
+      // min-term k-steps
+      const uint32_t id_min = id_qk | (1u << 7) | (1u << 10);
       const uint32_t id_pv = tc::idesc(128, 256, 0, 1);   // A (tensor memory), B MN-major
       auto tile_ready = [&](int i) {
         const bool r2 = wait(bar(kBarAFull + i % kNB), (i / kNB) & 1, abort_flag, a.err);
@@ -636,21 +751,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t kq0 = tc::desc(tc::su32(sA), 16, 1024);
       const uint64_t kp0 = tc::desc(tc::su32(sA), kPlane, 1024);
       const uint64_t qr0 = tc::desc(tc::su32(sQR), 16, 1024);
+      // (loops kept rolled: the issue rate is set by the tensor core, and the
+      // kernel's per-tile code has to stay small for the instruction caches)
       auto issue_qk = [&](int i) {
         const uint64_t d = kq0 + (uint64_t)(((i % kNB) * kABuf) >> 4);
-        int acc = 0;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t qa = tmem + kColQ + 32 * j + 8 * ks;
-            mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, acc);
+            mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, (j | ks) != 0);
             mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
-            acc = 1;
           }
         }
         // this rank's half of the RoPE channels: k-steps 2r, 2r + 1
-#pragma unroll
+#pragma unroll 1
         for (int k2 = 0; k2 < 2; ++k2) {
           const int ks = 2 * r + k2;
           tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
@@ -658,11 +773,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
                   d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
         }
+        // the min terms: the other rank's RoPE k-steps, in bf16
+#pragma unroll 1
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int ks = 2 * (1 - r) + k2;
+          tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                  d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+        }
         tc::commit(bar(kBarDFull));
       };
       auto issue_pv = [&](int i) {
         const uint64_t d = kp0 + (uint64_t)(((i % kNB) * kABuf) >> 4);
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < 4; ++ks) {
           // the four content groups' planes side by side: N = 256 channels
           const uint64_t b1 = d + (uint64_t)((2048 * ks) >> 4);
@@ -675,19 +797,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::commit(bar(kBarPFree));
         tc::commit(bar(kBarAFree + i % kNB));
       };
-      bool ok = n_tiles > 0 && tile_ready(0);
-      if (ok) issue_qk(0);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        if (i + 1 < n_tiles) {
-          ok = tile_ready(i + 1) && wait(bar(kBarDFree), i & 1, abort_flag, a.err);
+      // step k: QK of tile k (once its planes are in and the softmax warps
+      // have read tile k-1's logits), then PV of tile k-1
+      bool ok = true;
+      for (int k = 0; ok && k <= n_tiles; ++k) {
+        if (k < n_tiles) {
+          ok = tile_ready(k) && (k == 0 || wait(bar(kBarDFree), (k - 1) & 1, abort_flag, a.err));
           if (!ok) break;
           tc::tc_fence_after();
-          issue_qk(i + 1);
+          issue_qk(k);
         }
-        ok = wait(bar(kBarPFull), i & 1, abort_flag, a.err);
-        if (!ok) break;
-        tc::tc_fence_after();
-        issue_pv(i);
+        if (k >= 1) {
+          ok = wait(bar(kBarPFull), (k - 1) & 1, abort_flag, a.err);
+          if (!ok) break;
+          tc::tc_fence_after();
+          issue_pv(k - 1);
+        }
       }
       // drain (bounded, regardless of the abort flag) before TMEM is freed
       tc::commit(bar(kBarFlush));
@@ -734,67 +859,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // after an acquire on its plane-ready barrier (complete by now: QK ran).
       if (ok) ok = wait(bar(kBarDFull), i & 1, abort_flag, a.err);
       if (ok) ok = wait(bar(kBarAFull + buf), (i / kNB) & 1, abort_flag, a.err);
-      const uint32_t vmask = sMask[buf * 4 + 2 * th] | (sMask[buf * 4 + 2 * th + 1] << 16);
+      const uint32_t mk0 = sMask[buf * 4 + 2 * th], mk1 = sMask[buf * 4 + 2 * th + 1];
+      const bool shifted = ((mk0 | mk1) >> 31) != 0;  // some token's logit and P take a factor 16
+      uint32_t vmask = (mk0 & 0xFFFFu) | ((mk1 & 0xFFFFu) << 16);
       ok = warp_all(ok);
       if (ok) {
         tc::tc_fence_after();
         tmem_ld32(tl + kColD + kTW * th, S);
         tc::tc_fence_before();
         tc::bar_arrive(bar(kBarDFree));
-#pragma unroll
-        for (int t4 = 0; t4 < kTW / 4; ++t4) {
-          const float4 f = f4[t4];
-          S[4 * t4] *= f.x;
-          S[4 * t4 + 1] *= f.y;
-          S[4 * t4 + 2] *= f.z;
-          S[4 * t4 + 3] *= f.w;
-        }
-        // min terms: the content groups, and (rank 1) the RoPE group
-#pragma unroll
-        for (int j = 0; j < kMaxOwn; ++j) {
-          if (j >= n_own) break;
-          const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64);
-#pragma unroll
-          for (int t4 = 0; t4 < kTW / 4; ++t4) {
-            const float4 mv = m4[t4];
-            S[4 * t4] = fmaf(mv.x, qs[j], S[4 * t4]);
-            S[4 * t4 + 1] = fmaf(mv.y, qs[j], S[4 * t4 + 1]);
-            S[4 * t4 + 2] = fmaf(mv.z, qs[j], S[4 * t4 + 2]);
-            S[4 * t4 + 3] = fmaf(mv.w, qs[j], S[4 * t4 + 3]);
-          }
-        }
+        // the accumulator holds the min terms too (scaled like the planes)
+        if (shifted) scale_by_token(S, f4);
       }
       // exchange with the peer: my partial of my kTW tokens goes to the
       // peer's buffer (once the peer has read the previous tile's), the peer's
       // partial of the same tokens arrives in mine
       if (ok && i >= 1) ok = bar_wait_cluster(bar(kBarXFree + sw_idx), (i - 1) & 1, abort_flag, a.err);
       if (ok) {
-        const uint32_t dst = x_peer + (uint32_t)((th * kRows + h) * kXStride) * 4u;
 #pragma unroll
         for (int k = 0; k < kTW / 4; ++k)
-          st_async4(dst + 16 * k, S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3], xfull_peer);
+          st_async4(x_peer + (uint32_t)(((th * 8 + k) * kRows + h) * 16), S[4 * k], S[4 * k + 1],
+                    S[4 * k + 2], S[4 * k + 3], xfull_peer);
         if (lane == 0) expect_tx(bar(kBarXFull + sw_idx), 32 * kTW * 4);
         ok = wait(bar(kBarXFull + sw_idx), i & 1, abort_flag, a.err);
       }
       if (ok) {
-        const float4* src = reinterpret_cast<const float4*>(sX + (th * kRows + h) * kXStride);
+        const float4* src = reinterpret_cast<const float4*>(sX);
 #pragma unroll
         for (int k = 0; k < kTW / 4; ++k) {
-          const float4 v = src[k];
+          const float4 v = src[(th * 8 + k) * kRows + h];
           S[4 * k] += v.x;
           S[4 * k + 1] += v.y;
           S[4 * k + 2] += v.z;
           S[4 * k + 3] += v.w;
         }
       }
-      // validity, log2 scale, tile max over both halves
-      const int tok0 = bf_first + (i - n_pk) * 64 + kTW * th;  // bf16 tiles
+      // validity, log2 scale, tile max over both halves.  In bf16 tiles the
+      // row's query block also masks the last protected tokens.
+      if (!packed_tile) {
+        const int lim = sw.n_tok - n_masked - (bf_first + (i - n_pk) * 64 + kTW * th);
+        vmask &= lim <= 0 ? 0u : lim >= kTW ? 0xFFFFFFFFu : (1u << lim) - 1u;
+      }
       float mx = -INFINITY;
 #pragma unroll
       for (int t = 0; t < kTW; ++t) {
-        const bool v = packed_tile ? ((vmask >> t) & 1u) != 0
-                                   : (tok0 + t < bf_end && tok0 + t < sw.n_tok - n_masked);
-        S[t] = v ? S[t] * a.scale_log2 : -INFINITY;
+        S[t] = ((vmask >> t) & 1u) ? S[t] * a.scale_log2 : -INFINITY;
         mx = fmaxf(mx, S[t]);
       }
       sMax[((i & 1) * 2 + th) * kRows + h] = mx;
@@ -834,31 +943,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         lsum += S[t];
       }
       l += lsum;
-      // min terms of my four PV groups (unscaled P)
-#pragma unroll
+      // min terms of my four PV groups (unscaled P).  The loop stays rolled
+      // (the per-tile code of all warp roles has to fit the instruction
+      // caches): the four sums rotate one place per group, back in order
+      // after the fourth.
+#pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64);
-        float am = 0.f;
+        float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int t4 = 0; t4 < kTW / 4; ++t4) {
           const float4 mv = m4[t4];
-          am = fmaf(S[4 * t4], mv.x, am);
-          am = fmaf(S[4 * t4 + 1], mv.y, am);
-          am = fmaf(S[4 * t4 + 2], mv.z, am);
-          am = fmaf(S[4 * t4 + 3], mv.w, am);
+          am[0] = fmaf(S[4 * t4], mv.x, am[0]);
+          am[1] = fmaf(S[4 * t4 + 1], mv.y, am[1]);
+          am[2] = fmaf(S[4 * t4 + 2], mv.z, am[2]);
+          am[3] = fmaf(S[4 * t4 + 3], mv.w, am[3]);
         }
-        accm[j] += am;
+        const float a0 = accm[0] + ((am[0] + am[1]) + (am[2] + am[3]));
+        accm[0] = accm[1];
+        accm[1] = accm[2];
+        accm[2] = accm[3];
+        accm[3] = a0;
       }
       // P (times each token's plane factor) as fp16 high and low parts
       if (ok) {
         tc::tc_fence_after();
         uint32_t hi[kTW / 2], lo[kTW / 2];
+        if (shifted) scale_by_token(S, f4);
 #pragma unroll
-        for (int t4 = 0; t4 < kTW / 4; ++t4) {
-          const float4 f = f4[t4];
-          split_trunc(S[4 * t4] * f.x, S[4 * t4 + 1] * f.y, hi[2 * t4], lo[2 * t4]);
-          split_trunc(S[4 * t4 + 2] * f.z, S[4 * t4 + 3] * f.w, hi[2 * t4 + 1], lo[2 * t4 + 1]);
-        }
+        for (int t2 = 0; t2 < kTW / 2; ++t2) split_trunc(S[2 * t2], S[2 * t2 + 1], hi[t2], lo[t2]);
         tmem_st16_nowait(tl + kColP + (kTW / 2) * th, hi);
         tmem_st16_nowait(tl + kColP + 32 + (kTW / 2) * th, lo);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
