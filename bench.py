@@ -491,7 +491,7 @@ def run_table9(args):
     for B in (8, 32):
         for L in TABLE9_CONTEXTS:
             res = {}
-            for cb in (4, 16):
+            for cb in [c for c in (4, 16) if ("c4r4" if c == 4 else "bf16") in args.sweep_layouts]:
                 w = syn.custom(f"t9_b{B}_l{L}_c{cb}", [L] * B, heads=heads, content_bits=cb,
                                rope_bits=4 if cb == 4 else 16, seed=9)
                 table, npages = syn.make_paging(w)
@@ -537,7 +537,7 @@ def run_table9(args):
                     "hbm_frac": round(by / (med * 1e-6) / 1e9 / peak, 4),
                     "peak_source": f"{peak_kind} hbm_gbs",
                     "c4r4_vs_bf16_pct": (round(100.0 * (res[4] - med) / med, 1)
-                                         if cb == 16 else None)}), flush=True)
+                                         if cb == 16 and 4 in res else None)}), flush=True)
                 del cache, ws, out, q
                 torch.cuda.empty_cache()
 
@@ -640,6 +640,8 @@ def main():
     ap.add_argument("--sweep-workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS),
                     help="workload of the multi-query sweep")
     ap.add_argument("--sweep-reps", type=int, default=15)
+    ap.add_argument("--sweep-layouts", default="c4r4,bf16",
+                    help="table9 sweep: comma-separated layouts to time (c4r4, bf16)")
     args = ap.parse_args()
     if args.sweep == "table9":
         run_table9(args)
