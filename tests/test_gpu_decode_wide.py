@@ -201,3 +201,43 @@ def test_wide_two_row_blocks_mtp_128_heads(cb):
         for i in range(n):
             check_attention(out[b, i], ref[i], f"seq {b} (L={L}) query {i}")
             assert np.allclose(lse[b, i], ref_lse[i], rtol=0, atol=1e-4), f"lse seq {b} query {i}"
+
+
+@pytest.mark.parametrize("heads", [128, 16])
+def test_min_terms_with_q_group_sums_beyond_fp16(heads):
+    # Content q near 1100, so each group's q sum (the factor of the logits'
+    # min terms) is ~70,400, past the fp16 maximum, over a cache of values
+    # 0.05 +- 1e-3 (m' ~ 0.05).  The min terms then carry ~2,000 of each
+    # scaled logit and move it by O(1) from token to token (the oracle's
+    # softmax spreads over ~550 effective tokens, top weight ~1.6 %).  The
+    # 128-row kernel computes them on the tensor core from three bf16 parts
+    # per factor, the 16-head kernel (the control) in fp32.  The log-sum-exp
+    # (~2,039) is the sensitive check: fp32 sums of min terms of ~3,500 each
+    # leave ~1e-4 in it, so the bar is 1e-3.
+    import torch
+    import bit_mla_kv_lowbit_gb300 as pkg
+    rng = np.random.default_rng(94)
+    L = 900
+    ckv = 0.05 + rng.uniform(-1e-3, 1e-3, (L, 512))
+    kr = rng.standard_normal((L, 64))
+    q = np.concatenate([1100.0 + 10.0 * rng.standard_normal((heads, 512)),
+                        1e-3 * rng.standard_normal((heads, 64))], axis=1)
+    to_bits = lambda x: syn.bf16_bits_from_f32(np.asarray(x, dtype=np.float32))
+    ckv_b, kr_b, q_b = to_bits(ckv), to_bits(kr), to_bits(q)
+    table = np.arange(16, dtype=np.int32)[None, :]
+    cache = pkg.PagedCache(4, 4, table, 16, "cuda")
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    cache.write(to_dev(ckv_b, torch.bfloat16), to_dev(kr_b, torch.bfloat16),
+                torch.arange(L, dtype=torch.int32, device="cuda"),
+                seq_idx=torch.zeros(L, dtype=torch.int32, device="cuda"), seq_lens_after=lens)
+    scale = 1.0 / np.sqrt(192.0)
+    lse = torch.empty(1, heads, dtype=torch.float32, device="cuda")
+    out = cache.decode(to_dev(q_b[None], torch.bfloat16), lens, [L], scale, lse=lse)
+    torch.cuda.synchronize()
+    assert cache.error() == 0
+    got = out.cpu().numpy()[0]
+    model = oracle.PagedCacheModel(oracle.Layout(4, 4), 16, table)
+    model.write(np.zeros(L, np.int64), np.arange(L), ckv_b, kr_b, np.array([L]))
+    ref, ref_lse = oracle.mla_decode_fp64(q_b, model.effective_keys(0, L), scale)
+    check_attention(got, ref, f"{heads} heads")
+    assert np.allclose(lse.cpu().numpy()[0], ref_lse, rtol=0, atol=1e-3)
