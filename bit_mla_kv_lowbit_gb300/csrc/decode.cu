@@ -149,8 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
   // n_masked tokens (all inside the recent window)
   const int n_masked = a.n_q - 1 - (hc * kHC) / (a.H / a.n_q);
 
-  // Copy packed page `tile_i` of this split into the team's staging buffer.
-  auto stage_page = [&](int tile_i) {
+  // Copy part of packed page `tile_i` of this split into the team's staging
+  // buffer: the thread's 16-byte chunks ttid + kTeamThreads * i for i in
+  // [i0, i1).  The whole page is the parts i in [0, kStageIters); a commit
+  // closes it.
+  constexpr int kStageIters = (G.page_bytes / 16 + kTeamThreads - 1) / kTeamThreads;
+  auto stage_part = [&](int tile_i, int i0, int i1) {
     if constexpr (kPacked) {
       const long long page = s_pages[tile_i];
       if (page >= 0 && page < a.num_pages) {
@@ -158,7 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
         constexpr int kChunks = G.page_bytes / 16;
         constexpr int kRowChunks = G.content_row / 16;
         constexpr int kContentChunks = kPageTokens * kRowChunks;
-        for (int k = ttid; k < kChunks; k += kTeamThreads) {
+        for (int i = i0; i < i1; ++i) {
+          const int k = ttid + kTeamThreads * i;
+          if (k >= kChunks) break;
           int dst = k * 16;
           if (k < kContentChunks) {
             const int r = k / kRowChunks, c = k % kRowChunks;
@@ -168,6 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
         }
       }
     }
+  };
+  auto stage_page = [&](int tile_i) {
+    stage_part(tile_i, 0, kStageIters);
     cp_async_commit();
   };
 
@@ -468,8 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       smax[warp * kHC + h0 + 8] = mx1;
     }
     team_sync(team);
-    // the staging buffer is free again: fetch this team's next page
-    if (kPacked && tile_i + kTeams < n_pages) stage_page(tile_i + kTeams);
+    // the staging buffer is free again: this team's next page is fetched in
+    // parts between the PV k-steps below, where the copies overlap the MMAs
+    // instead of stalling every warp of the team on the load/store queue
+    const bool stage_next = kPacked && tile_i + kTeams < n_pages;
     float t0 = -INFINITY, t1 = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kTeamWarps; ++w) {
@@ -514,6 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
+        constexpr int kPart = (kStageIters + 2) / 3;
+        if (stage_next && ks < 3)
+          stage_part(tile_i + kTeams, kPart * ks, min(kPart * (ks + 1), kStageIters));
         const int t = ks * 16 + 2 * j;
         const float2 pa = *reinterpret_cast<const float2*>(&P[h0 * kPStride + t]);
         const float2 pb = *reinterpret_cast<const float2*>(&P[(h0 + 8) * kPStride + t]);
@@ -545,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
         }
       }
     }
+    cp_async_commit();  // the next page's parts (an empty group when none)
   }
 
   // ---- epilogue: finish the min term, merge the two teams, write the partial
