@@ -55,6 +55,7 @@ constexpr int kTOffS = kTOffP + kHC * kPStride * 4;
 constexpr int kTOffM = kTOffS + 8 * kPageTokens * 4;
 constexpr int kTOffMax = kTOffM + 8 * kPageTokens * 4;
 constexpr int kTOffStage = kTOffMax + kTeamWarps * kHC * 4;
+static_assert(kTOffMax % 16 == 0, "tile maxima are read as float4");
 __host__ __device__ constexpr int team_bytes(int cbits) {
   return kTOffStage + (cbits == 16 ? 0 : page_geom(cbits).page_bytes);
 }
@@ -472,20 +473,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(DecodeArgs a)
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
-    if (j == 0) {
-      smax[warp * kHC + h0] = mx0;
-      smax[warp * kHC + h0 + 8] = mx1;
+    if (j == 0) {  // [head][warp]: a head's 8 warp maxima are two 16-byte words
+      smax[h0 * kTeamWarps + warp] = mx0;
+      smax[(h0 + 8) * kTeamWarps + warp] = mx1;
     }
     team_sync(team);
     // the staging buffer is free again: this team's next page is fetched in
     // parts between the PV k-steps below, where the copies overlap the MMAs
     // instead of stalling every warp of the team on the load/store queue
     const bool stage_next = kPacked && tile_i + kTeams < n_pages;
-    float t0 = -INFINITY, t1 = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kTeamWarps; ++w) {
-      t0 = fmaxf(t0, smax[w * kHC + h0]);
-      t1 = fmaxf(t1, smax[w * kHC + h0 + 8]);
+    float t0, t1;
+    {
+      static_assert(kTeamWarps == 8, "two float4 per head");
+      const float4* r0 = reinterpret_cast<const float4*>(smax + h0 * kTeamWarps);
+      const float4* r1 = reinterpret_cast<const float4*>(smax + (h0 + 8) * kTeamWarps);
+      const float4 a0 = r0[0], b0 = r0[1], a1 = r1[0], b1 = r1[1];
+      t0 = fmaxf(fmaxf(fmaxf(a0.x, a0.y), fmaxf(a0.z, a0.w)), fmaxf(fmaxf(b0.x, b0.y), fmaxf(b0.z, b0.w)));
+      t1 = fmaxf(fmaxf(fmaxf(a1.x, a1.y), fmaxf(a1.z, a1.w)), fmaxf(fmaxf(b1.x, b1.y), fmaxf(b1.z, b1.w)));
     }
     const float mn0 = fmaxf(m_run0, t0), mn1 = fmaxf(m_run1, t1);
     const float alpha0 = mn0 == -INFINITY ? 1.f : fast_exp2(m_run0 - mn0);
