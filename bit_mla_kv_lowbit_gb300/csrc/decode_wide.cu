@@ -294,8 +294,9 @@ __device__ __forceinline__ void scale_parts(uint32_t s16, bool shift, uint32_t& 
 }
 
 // Min terms on the tensor core.  The logit's min terms sum_j qs_j m'_j over
-// the CTA's groups (qs_j: the row's q summed over group j; m'_j: the token's
-// dequantised value at code 0 of group j) run as two bf16 k-steps of QK, in
+// the CTA's groups (qs_j: the row's q summed over group j; m'_j = m + centre s:
+// the token's dequantised value at the centre code of group j, where the
+// planes' centred codes are 0) run as two bf16 k-steps of QK, in
 // the RoPE k-steps this rank leaves unused (both in the RoPE q block and in
 // the RoPE s_hi plane).  Each factor is split in three bf16 parts (h + m + l,
 // 24 significant bits; bf16 has the fp32 exponent range), and the two
