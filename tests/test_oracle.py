@@ -274,6 +274,62 @@ def test_hadamard_rotation_closed_forms():
     assert np.all(err <= 6 * 2.0 ** -24 * np.abs(xb).astype(np.float64).sum(axis=1, keepdims=True))
 
 
+# ---------------------------------------------------------------- bf16 rounding
+
+@pytest.mark.parametrize("x, want", [
+    (1.0 + 2.0 ** -8, 0x3F80),                   # tie -> even mantissa (down to 1.0)
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),               # tie -> even mantissa (up to 1 + 2^-6)
+    (1.0 + 2.0 ** -8 + 2.0 ** -20, 0x3F81),      # just above the tie -> up
+    (1.0 + 2.0 ** -8 - 2.0 ** -20, 0x3F80),      # just below the tie -> down
+    (-(1.0 + 2.0 ** -8), 0xBF80),
+    (-(1.0 + 3 * 2.0 ** -8), 0xBF82),
+    (0.0, 0x0000),
+    (-0.0, 0x8000),
+    (2.0 ** -126, 0x0080),                       # smallest normal
+    (2.0 ** -130, 0x0008),                       # subnormal, exact in bf16
+    (3.0 * 2.0 ** -134, 0x0000 + 2),             # subnormal tie (1.5 ulp) -> 2 (even)
+    (65504.0, 0x4780),                           # 65504 = 1.999 x 2^15 rounds up to 65536
+])
+def test_f32_to_bf16_bits_textbook(x, want):
+    # the rotation's bf16 rounding: nearest, ties to even (textbook bf16 facts)
+    got = oracle.quant.f32_to_bf16_bits(np.array([x], dtype=np.float32))[0]
+    assert int(got) == want
+    # the input generator's rounding obeys the same facts
+    assert int(bf16(np.array([x]))[0]) == want
+
+
+def test_f32_to_bf16_bits_matches_torch():
+    # an independent implementation of the same IEEE rounding: torch's
+    # float32 -> bfloat16 conversion, over many magnitudes and both signs
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-60, 60, 200000))).astype(np.float32)
+    # ties: random finite high halves (exponent below 0xFF) with the low 16 bits
+    # exactly 0x8000
+    ties = ((rng.integers(0, 0x7F7F, 20000).astype(np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.quant.f32_to_bf16_bits(x), want)
+    assert np.array_equal(bf16(x), want)
+
+
+def test_rotate_latent_bits_rounds_a_hand_derived_group():
+    # x = e_0 + (3/256) e_1 in every content group.  Every butterfly stage only
+    # copies sums: element i becomes 1 + 3/256 (i even) or 1 - 3/256 (i odd),
+    # exact in float32; the 1/8 scale is exact too.  Rounded to bf16:
+    #   (1 + 3/256) / 8 = 1.00000011b x 2^-3: a tie between mantissas 0000001
+    #       and 0000010 -> even -> 1.0000010b x 2^-3 = bits 0x3E02;
+    #   (1 - 3/256) / 8 = 253/2048 = 1.1111101b x 2^-4: exact -> bits 0x3DFD.
+    x = np.zeros((2, 512), dtype=np.float32)
+    x[:, 0::64] = 1.0
+    x[:, 1::64] = 3.0 / 256.0
+    x[1] = -x[1]
+    got = oracle.rotate_latent_bits(bf16(x))
+    want = np.where(np.arange(512) % 2 == 0, 0x3E02, 0x3DFD).astype(np.uint16)
+    assert np.array_equal(got[0], want)
+    assert np.array_equal(got[1], want | 0x8000)
+
+
 def test_rotated_attention_equals_unrotated_on_exact_keys():
     # keys stored in the rotated basis (exactly, in float64) must give the same
     # logits and outputs as the plain keys: q is rotated, the output rotated back
