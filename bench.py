@@ -334,9 +334,10 @@ def run_gpu(args, w):
     tpk, tpk_kind = tensor_peak()
     dec_tflops = algorithmic_flops(w, s.lens) / (t_dec * 1e-3) / 1e12
     trec = traffic_record(f"decode_{w.name}")
-    # split + combine; the append is fused into the default split kernel, the
-    # other kernels (MLA_LOWBIT_DECODE) run the writer kernel first
-    fused = w.writer_in_step and os.environ.get("MLA_LOWBIT_DECODE", "m")[:1] in ("", "m")
+    # split + combine; the library fuses the append into the split kernel for
+    # packed caches whose rows are not a multiple of 128 (the 128-row kernel
+    # and bf16 pages run the writer kernel first)
+    fused = w.writer_in_step and w.content_bits != 16 and w.heads % 128 != 0
     n_launch_step = 2 + (1 if w.writer_in_step and not fused else 0)
     kernel_desc = ("append + decode (split kernel with fused append, combine)"
                    if w.writer_in_step else "decode (split + combine)")

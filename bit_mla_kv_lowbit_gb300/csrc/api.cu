@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -44,6 +45,25 @@ int device_sm_count() {
 }
 
 }  // namespace
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  // (device, kernel, bytes) triples already applied; a handful of kernels per device
+  struct Entry { int dev; const void* kernel; int bytes; };
+  static Entry done[256];
+  static int n_done = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].dev == dev && done[i].kernel == kernel && done[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (n_done < 256) done[n_done++] = Entry{dev, kernel, bytes};
+  return cudaSuccess;
+}
+
 }  // namespace mlalb
 
 using namespace mlalb;

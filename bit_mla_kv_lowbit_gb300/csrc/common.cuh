@@ -181,9 +181,10 @@ bool decode_fuses_append(int cbits, int rotate, int rows);
 // 128-row block for the tcgen05 kernel): the planner sizes chunks so that all
 // fit one wave.
 int decode_ctas_per_split(int cbits, int rows, int rotate);
-cudaError_t launch_decode_tc(int cbits, const DecodeArgs& a, cudaStream_t stream);
-cudaError_t launch_decode_hy(int cbits, const DecodeArgs& a, cudaStream_t stream);
-cudaError_t launch_decode_gw(int cbits, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stream);
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (device, kernel): the limit is a per-device attribute.
+// Thread-safe.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
 }  // namespace mlalb

@@ -23,10 +23,10 @@
 // * The contraction dimension is permuted inside each group so that the
 //   unpack's natural pair order is the mma fragment order; q is staged in the
 //   same permuted order and the output channels are un-permuted at the end.
-// * The sink/recent bf16 tokens are one more split of the same sequence, so
-//   the combine kernel folds them into the one softmax.
+// * The sink/recent bf16 tokens are more 64-token tiles of the same split
+//   work list (after the sequence's pages, see split_work), so the combine
+//   kernel folds them into the one softmax.
 #include <cfloat>
-#include <cstdlib>
 
 #include "decode_common.cuh"
 #include "writer_common.cuh"
@@ -756,44 +756,26 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, combine_kernel, ca);
 }
 
-// Kernel for a layout and a row count (n_q * heads): packed caches with a
-// multiple of 128 rows and no rotation take the 2-CTA tcgen05 kernel
-// (decode_wide.cu, one cluster per split and 128-row block); everything else
-// the mma.sync kernel above (the fastest
-// measured on GB300 for 16-head chunks).  MLA_LOWBIT_DECODE overrides the
-// choice: "m" always the mma.sync kernel; for packed single-query
-// unrotated decodes "h" the hybrid mma.sync + tcgen05 kernel (decode_hy.cu),
-// "t" the all-tcgen05 16-head kernel (decode_tc.cu), "g" the group-per-warp
-// kernel (decode_gw.cu).
-enum class SplitKernel { kMma, kHybrid, kTc, kGroupWarp, kWide };
-static SplitKernel split_kernel(int cbits, int n_q, int rotate, int rows) {
-  const char* v = getenv("MLA_LOWBIT_DECODE");
-  const char k = v ? v[0] : 0;
-  if (k == 0 && cbits != 16 && !rotate && rows % 128 == 0) return SplitKernel::kWide;
-  // the only one with query blocks and with rotated queries
-  if (cbits == 16 || n_q > 1 || rotate) return SplitKernel::kMma;
-  if (k == 'h') return SplitKernel::kHybrid;
-  if (k == 't') return SplitKernel::kTc;
-  if (k == 'g') return SplitKernel::kGroupWarp;
-  return SplitKernel::kMma;
+// Kernel for a layout and a row count (n_q * heads), fixed by those alone:
+// packed caches with a multiple of 128 rows and no rotation take the 2-CTA
+// tcgen05 kernel (decode_wide.cu, one cluster per split and 128-row block);
+// everything else the mma.sync kernel above in 16-row chunks.
+static bool use_wide(int cbits, int rotate, int rows) {
+  return cbits != 16 && !rotate && rows % 128 == 0;
 }
 
 int decode_ctas_per_split(int cbits, int rows, int rotate) {
-  return split_kernel(cbits, 1, rotate, rows) == SplitKernel::kWide ? 2 * (rows / 128) : rows / kHC;
+  return use_wide(cbits, rotate, rows) ? 2 * (rows / 128) : rows / kHC;
 }
 
 bool decode_fuses_append(int cbits, int rotate, int rows) {
-  return cbits != 16 && split_kernel(cbits, 1, rotate, rows) == SplitKernel::kMma;
+  return cbits != 16 && !use_wide(cbits, rotate, rows);
 }
 
 cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse,
                           cudaStream_t stream) {
-  const SplitKernel sk = split_kernel(cbits, a.n_q, a.rotate, a.H);
-  if (sk != SplitKernel::kMma) {
-    cudaError_t et = sk == SplitKernel::kTc       ? launch_decode_tc(cbits, a, stream)
-                     : sk == SplitKernel::kHybrid ? launch_decode_hy(cbits, a, stream)
-                     : sk == SplitKernel::kWide   ? launch_decode_wide(cbits, a, stream)
-                                                  : launch_decode_gw(cbits, a, stream);
+  if (use_wide(cbits, a.rotate, a.H)) {
+    const cudaError_t et = launch_decode_wide(cbits, a, stream);
     if (et != cudaSuccess) return et;
     CombineArgs ca{a.part_o, a.part_ml, a.seq_split, out, lse, a.B, a.H, a.total_splits, 0};
     return launch_combine(ca, stream);
@@ -803,14 +785,8 @@ cudaError_t launch_decode(int cbits, const DecodeArgs& a, float* out, float* lse
                              : cbits == 2 ? (rot ? decode_split_kernel<2, true> : decode_split_kernel<2, false>)
                                           : decode_split_kernel<16, false>;
   const int smem = smem_bytes(cbits, rot);
-  static bool configured[5] = {false, false, false, false, false};
-  const int k = cbits == 16 ? 4 : (cbits == 4 ? 0 : 2) + (rot ? 1 : 0);
-  cudaError_t e = cudaSuccess;
-  if (!configured[k]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[k] = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.total_splits, a.H / kHC), block(kThreads);
   kern<<<grid, block, smem, stream>>>(a);
   e = cudaGetLastError();

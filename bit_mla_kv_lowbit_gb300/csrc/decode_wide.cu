@@ -1034,23 +1034,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace wide
 
 cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stream) {
-  static bool configured[2] = {false, false};
-  const int k = cbits == 4 ? 0 : 1;
   const int smem = wide::kSmem + 1024;
-  cudaError_t e = cudaSuccess;
-  if (!configured[k]) {
-    e = cbits == 4 ? cudaFuncSetAttribute(wide::decode_wide_kernel<4>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                   : cudaFuncSetAttribute(wide::decode_wide_kernel<2>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[k] = true;
-  }
+  void (*kern)(DecodeArgs) = cbits == 4 ? wide::decode_wide_kernel<4> : wide::decode_wide_kernel<2>;
+  const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(2 * a.total_splits, a.H / wide::kRows), block(wide::kThreads);
-  if (cbits == 4)
-    wide::decode_wide_kernel<4><<<grid, block, smem, stream>>>(a);
-  else
-    wide::decode_wide_kernel<2><<<grid, block, smem, stream>>>(a);
+  kern<<<grid, block, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -138,12 +138,15 @@ int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* 
                      int max_pages, void* page_pool, int64_t num_pages, void* sink_buf,
                      void* recent_buf, int32_t* err_word, void* stream);
 
-/* Split-KV plan of one decode call.  Pages of each sequence are cut into
- * splits of `chunk_pages` pages (chosen from the total work and the SM count,
- * at most 64 so that no split accumulates more than 4096 tokens);
- * packed layouts add one split per sequence for its bf16 tokens.  Writes the
- * number of splits and the workspace bytes the call needs.  num_sms == 0 asks
- * the current CUDA device. */
+/* Split-KV plan of one decode call.  The work of a sequence is a list of
+ * units: one per 64-token page that holds a packed-served token (bf16 pages:
+ * every page), then, for packed layouts, its protected bf16 tokens (sink and
+ * recent) in 64-token tiles of 3 units each.  The list is cut into splits of
+ * `chunk_pages` units, chosen from the total work and the SM count so that all
+ * splits of the call fit one wave when they can, and at most 64 so that no
+ * split accumulates more than 4096 tokens; a bf16 tile belongs to the split
+ * that holds its first unit.  Writes the number of splits and the workspace
+ * bytes the call needs.  num_sms == 0 asks the current CUDA device. */
 int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int heads,
                            const int32_t* seq_lens_host, int num_sms, int* total_splits,
                            int* chunk_pages, size_t* workspace_bytes);
@@ -174,11 +177,10 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
  *   workspace     at least the bytes mla_lowbit_decode_plan reports
  *   err_word      int32 (device), OR-ed MLA_LOWBIT_DEV_* bits
  * Launches the split kernel and the log-sum-exp combine kernel on `stream`.
- * The split kernel runs on mma.sync tensor-core instructions.  For packed
- * layouts the environment variable MLA_LOWBIT_DECODE, read at call time,
- * selects another split kernel with the same results within the stated
- * tolerance: "hy" (QK on mma.sync, PV on tcgen05 with tensor-memory
- * accumulators) or "tc" (QK and PV on tcgen05). */
+ * The split kernel is fixed by the layout and the row count: packed,
+ * unrotated layouts with a multiple of 128 rows per sequence run on tcgen05
+ * tensor cores as 2-CTA clusters; every other call runs on mma.sync
+ * tensor-core instructions in 16-row chunks. */
 int mla_lowbit_decode(const mla_lowbit_layout* layout, int num_seqs, int heads,
                       float softmax_scale, const void* q, const void* page_pool,
                       int64_t num_pages, const int32_t* block_table, int max_pages,
@@ -225,7 +227,8 @@ int mla_lowbit_write_decode(const mla_lowbit_layout* layout, int num_seqs, int h
  *   out    [num_seqs][n][heads][512] float32; lse [num_seqs][n][heads] or NULL
  *   seq_lens_host entries >= n
  *   workspace  mla_lowbit_decode_plan with heads = n * heads
- * Always runs on the mma.sync split kernel. */
+ * The split kernel is chosen as for mla_lowbit_decode from the row count
+ * n * heads (so 128-row blocks run on tcgen05). */
 int mla_lowbit_decode_multi(const mla_lowbit_layout* layout, int num_seqs, int queries_per_seq,
                             int heads, float softmax_scale, const void* q, const void* page_pool,
                             int64_t num_pages, const int32_t* block_table, int max_pages,

@@ -42,32 +42,6 @@ def test_wide_write_decode_steps():
         _check_run_step(run, s, lse=True, fused=True)
 
 
-def test_wide_matches_mma_kernel(monkeypatch):
-    # the same decode through the 16-head mma.sync kernel (forced by the
-    # environment) and through the 128-row kernel agree to the oracle's bar
-    import torch
-    w = syn.custom("wide_vs_mma", [2100, 5000, 140], heads=128, content_bits=4, seed=84)
-    run = GpuRun(w)
-    run.prefill()
-    ckv, kr, q = run.step_inputs(0)
-    lens = (run.lens).astype(np.int32)
-    run.cache.write(to_dev(ckv, torch.bfloat16), to_dev(kr, torch.bfloat16),
-                    to_dev(lens - 1, torch.int32), seq_lens_after=to_dev(lens, torch.int32))
-    outs = []
-    for env in (None, "m"):
-        if env:
-            monkeypatch.setenv("MLA_LOWBIT_DECODE", env)
-        else:
-            monkeypatch.delenv("MLA_LOWBIT_DECODE", raising=False)
-        out = run.cache.decode(to_dev(q, torch.bfloat16), to_dev(lens, torch.int32),
-                               [int(x) for x in lens], w.softmax_scale)
-        torch.cuda.synchronize()
-        outs.append(out.cpu().numpy())
-    assert run.cache.error() == 0
-    for b in range(w.batch):
-        check_attention(outs[0][b], outs[1][b].astype(np.float64), f"seq {b}")
-
-
 @pytest.mark.parametrize("cb,heads,n", [(4, 64, 2), (4, 16, 8), (2, 32, 4)])
 def test_wide_multi_query_blocks(cb, heads, n):
     # n_q * heads = 128 rows: per-row causal masks inside the 128-row kernel
