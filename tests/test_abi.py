@@ -177,6 +177,9 @@ def test_plan_fills_one_wave_on_uniform_lengths():
     # ceil(4152 / 152) = 28 -> 19 splits per sequence: one wave of 152 CTAs
     total, chunk, _ = pkg.decode_plan(pkg.layout(4, 4), 16, [32768] * 8, num_sms=152)
     assert (total, chunk) == (152, 28)
+    # bf16 pages: 8 x 512 pages in chunks of 27 -> 19 splits per sequence
+    total, chunk, _ = pkg.decode_plan(pkg.layout(16, 16), 16, [32768] * 8, num_sms=152)
+    assert (total, chunk) == (152, 27)
 
 
 def test_plan_spreads_work_over_full_waves():
@@ -187,7 +190,7 @@ def test_plan_spreads_work_over_full_waves():
     for heads, lens in [(128, [8192] * 32), (128, [131072] * 4), (128, [10240] * 32),
                         (16, [2000] * 1000), (16, [32768] * 8)]:
         total, chunk, _ = pkg.decode_plan(lay, heads, lens, num_sms=152)
-        cps = 2 if heads == 128 else heads // 16
+        cps = 2 * (heads // 128) if heads % 128 == 0 else heads // 16
         assert 1 <= chunk <= 64
         waves = -(-total * cps // 152)
         capped = sum(_expected_splits(L, True, 64) for L in lens)
