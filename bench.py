@@ -525,7 +525,11 @@ def run_table9(args):
                     e1.record()
                     torch.cuda.synchronize()
                     ts.append(e0.elapsed_time(e1) * 1e3)
-                assert cache.error() == 0, f"device error word {cache.error()}"
+                    # every call: a device-detected error (bad page, plan mismatch,
+                    # a bounded wait that ran out) fails the sweep
+                    err = cache.error()
+                    assert err == 0, f"device error word {err} (B={B}, L={L}, {cb}-bit)"
+                assert bool(torch.isfinite(out).all()), f"non-finite output (B={B}, L={L})"
                 by = algorithmic_bytes(w, np.full(B, L))["decode"]
                 med = sorted(ts)[len(ts) // 2]
                 res[cb] = med

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     load,
     page_bytes,
     read_error,
+    set_fault_injection,
     strerror,
     version,
     write,

@@ -28,6 +28,7 @@ EXPORTS = (
     "mla_lowbit_decode_noalloc",
     "mla_lowbit_write_decode",
     "mla_lowbit_decode_multi",
+    "mla_lowbit_set_fault_injection",
     "mla_lowbit_read_error",
     "mla_lowbit_strerror",
     "mla_lowbit_version",
@@ -89,6 +90,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_lowbit_decode_multi.argtypes = [lp, i32, i32, i32, ctypes.c_float, vp, vp, i64, vp,
                                             i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.mla_lowbit_decode_multi.restype = i32
+    lib.mla_lowbit_set_fault_injection.argtypes = [i32, i64]
+    lib.mla_lowbit_set_fault_injection.restype = i32
     lib.mla_lowbit_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_lowbit_read_error.restype = i32
     lib.mla_lowbit_strerror.argtypes = [i32]
@@ -322,6 +325,14 @@ def decode_noalloc(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_ho
         lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
         _ptr(lse), _ptr(err_word), _stream(stream))
     _check(st, "mla_lowbit_decode_noalloc")
+
+
+def set_fault_injection(mode: int, wait_cycles: int = 0) -> None:
+    """Self-test setting of the tcgen05 kernels' bounded waits (process-wide):
+    mode 1 withholds one hand-off so that the waits run out after
+    ``wait_cycles`` SM cycles (0 = the default limit); mode 0 is normal."""
+    _check(load().mla_lowbit_set_fault_injection(int(mode), int(wait_cycles)),
+           "mla_lowbit_set_fault_injection")
 
 
 def read_error(err_word) -> int:

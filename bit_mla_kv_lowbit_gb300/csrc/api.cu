@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/mla_lowbit.h: argument checks,
 // split planning and kernel launches.  No device memory is allocated here.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -31,6 +32,10 @@ int check_layout(const mla_lowbit_layout* l) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Self-test settings of the tcgen05 kernels' bounded waits (mla_lowbit_set_fault_injection).
+std::atomic<int> g_fault_mode{0};
+std::atomic<long long> g_wait_cycles{0};
 
 int device_sm_count() {
   static int cached[64] = {0};
@@ -254,6 +259,8 @@ static int decode_impl(const mla_lowbit_layout* layout, int num_seqs, int n_q, i
   a.chunk_pages = chunk;
   a.total_splits = total;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.fault = g_fault_mode.load();
+  if (const long long wc = g_wait_cycles.load(); wc > 0) a.wait_cycles = wc;
   if (fused) {
     a.new_ckv = static_cast<const uint32_t*>(ckv_new);
     a.new_kr = static_cast<const uint32_t*>(krope_new);
@@ -302,6 +309,13 @@ int mla_lowbit_decode_multi(const mla_lowbit_layout* layout, int num_seqs, int q
                      const_cast<void*>(page_pool), num_pages, block_table, max_pages, seq_lens,
                      seq_lens_host, const_cast<void*>(sink_buf), const_cast<void*>(recent_buf), out,
                      lse, workspace, workspace_bytes, err_word, stream);
+}
+
+int mla_lowbit_set_fault_injection(int mode, int64_t wait_cycles) {
+  if (mode < 0 || mode > 1 || wait_cycles < 0) return MLA_LOWBIT_EINVAL;
+  g_fault_mode.store(mode);
+  g_wait_cycles.store(wait_cycles);
+  return MLA_LOWBIT_OK;
 }
 
 int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out) {

@@ -161,6 +161,12 @@ struct DecodeArgs {
   // heads, query i at position seq_lens[b] - n_q + i (causal among them).
   int n_q = 1;
   int rotate = 0;  // the cache's content latent is stored rotated (layout field)
+  // Bounded waits of the tcgen05 kernels give up after this many SM clock
+  // cycles (about one second by default).  fault = 1 (self-test only) makes
+  // the 128-row kernel's unpack warps skip their first hand-off, so that the
+  // waits downstream of it run out.
+  long long wait_cycles = 2000000000LL;
+  int fault = 0;
   // Fused append (mla_lowbit_write_decode): the token at position
   // seq_lens[b] - 1 of every sequence, written by the sequence's bf16 split of
   // head chunk 0 and read from here by every bf16 split.  Null for a plain decode.

@@ -49,7 +49,7 @@ __device__ __forceinline__ void bar_arrive(uint32_t bar) {
 
 // Bounded wait on an mbarrier phase; on time-out raises the CTA abort flag.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                         int32_t* err) {
+                                         int32_t* err, long long limit = kWaitCycles) {
   const long long t0 = clock64();
   for (;;) {
     uint32_t ok;
@@ -61,7 +61,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile
         : "memory");
     if (ok) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       set_error(err, MLA_LOWBIT_DEV_PIPELINE);
       return false;
@@ -234,7 +234,7 @@ __device__ __forceinline__ void arrive_peer_relaxed(uint32_t bar_cluster_addr) {
 }
 // Bounded wait for arrivals from the peer that carry no data.
 __device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                 int32_t* err) {
+                                                 int32_t* err, long long limit = kWaitCycles) {
   const long long t0 = clock64();
   for (;;) {
     uint32_t ok;
@@ -246,7 +246,7 @@ __device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity, 
         : "memory");
     if (ok) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       set_error(err, MLA_LOWBIT_DEV_PIPELINE);
       return false;
@@ -257,7 +257,8 @@ __device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity, 
 // (up to kSuspendNs per try) instead of spinning, so waiting warps leave the
 // issue slots to the working ones.
 constexpr uint32_t kSuspendNs = 200000;
-__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* err) {
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* err,
+                                     long long limit = kWaitCycles) {
   const long long t0 = clock64();
   for (;;) {
     uint32_t ok;
@@ -269,7 +270,7 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int
         : "memory");
     if (ok) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       set_error(err, MLA_LOWBIT_DEV_PIPELINE);
       return false;

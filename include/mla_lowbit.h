@@ -265,6 +265,24 @@ int mla_lowbit_decode_noalloc(const mla_lowbit_layout* layout, int num_seqs, int
                               const void* sink_buf, const void* recent_buf, float* out,
                               float* lse, int32_t* err_word, void* stream);
 
+/* Self-test of the failure path of the tcgen05 decode kernels (the pages have
+ * no counterpart to it; it checks this library's own error handling).  Those
+ * kernels hand work between warp roles through mbarriers, and every wait on
+ * one is bounded: when it runs out the CTA sets MLA_LOWBIT_DEV_PIPELINE in the
+ * error word, its warps leave their loops together, the tensor-core work
+ * already issued drains, tensor memory is freed and the kernel returns (no
+ * trap, the context stays usable; the call's output is invalid).
+ *
+ * This sets, for every later decode call of the process (all threads):
+ *   mode        0: normal operation; 1: the 128-row (tcgen05) decode kernel's
+ *               unpack warps withhold their first hand-off, so that the waits
+ *               behind it run out -- a fault made on purpose, for tests only;
+ *   wait_cycles the wait limit in SM clock cycles; 0 restores the default
+ *               (about one second).
+ * Returns MLA_LOWBIT_EINVAL for a mode other than 0 or 1 or a negative limit.
+ * The mma.sync kernel has no such waits and ignores both settings. */
+int mla_lowbit_set_fault_injection(int mode, int64_t wait_cycles);
+
 /* Synchronously copies the device error word to *code_out (a blocking
  * cudaMemcpy: it waits for prior work on the legacy default stream). */
 int mla_lowbit_read_error(const int32_t* err_word, int32_t* code_out);

@@ -30,8 +30,40 @@ def to_dev(a, dtype, dev="cuda"):
     return t.to(dev).view(dtype)
 
 
+GUARD_BYTES = 4096
+GUARD_FILL = 0xA5
+
+
+class Guards:
+    """Device buffers with guard bytes before and after them: a kernel that
+    writes outside a buffer it is given changes a guard."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.dev = dev
+        self.regions = []
+
+    def alloc(self, shape, dtype, what):
+        torch = self.torch
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        n16 = (n + 15) // 16 * 16
+        full = torch.full((GUARD_BYTES + n16 + GUARD_BYTES,), GUARD_FILL, dtype=torch.uint8,
+                          device=self.dev)
+        self.regions.append((what, full, n))
+        return full[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(*shape)
+
+    def check(self):
+        for what, full, n in self.regions:
+            head = full[:GUARD_BYTES]
+            tail = full[GUARD_BYTES + n:]
+            assert bool((head == GUARD_FILL).all()), f"guard bytes before {what} overwritten"
+            assert bool((tail == GUARD_FILL).all()), f"guard bytes after {what} overwritten"
+
+
 class GpuRun:
-    """One workload on the GPU: prefill, then ``steps`` writer + decode steps."""
+    """One workload on the GPU: prefill, then ``steps`` writer + decode steps.
+    The page pool, bf16 buffers, outputs and workspace sit between guard bytes
+    (``guards.check()``)."""
 
     def __init__(self, w: syn.Workload, dev: str = "cuda", rotate: bool = False):
         import torch
@@ -44,9 +76,29 @@ class GpuRun:
         self.rotate = rotate
         self.cache = pkg.PagedCache(w.content_bits, w.rope_bits, self.table, self.npages, dev,
                                     rotate=rotate)
+        self.guards = Guards(torch, dev)
+        c = self.cache
+        c.pool = self.guards.alloc(tuple(c.pool.shape), torch.uint8, "page pool")
+        c.pool.zero_()
+        if c.sink is not None:
+            c.sink = self.guards.alloc(tuple(c.sink.shape), torch.bfloat16, "sink buffer")
+            c.recent = self.guards.alloc(tuple(c.recent.shape), torch.bfloat16, "recent buffer")
+            c.sink.zero_()
+            c.recent.zero_()
+        self.out = self.guards.alloc((w.batch, w.heads, 512), torch.float32, "output")
+        self.lse = self.guards.alloc((w.batch, w.heads), torch.float32, "lse")
+        self._ws = None
         self.scales = syn.channel_scales(w)
         self.tokens = {}
         self.step = -1
+
+    def workspace(self, lens_host):
+        """Guarded workspace for this run's row count, grown to the plan's size."""
+        import bit_mla_kv_lowbit_gb300 as pkg
+        _, _, nbytes = pkg.decode_plan(self.cache.layout, self.w.heads, lens_host)
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = self.guards.alloc((max(int(nbytes), 16),), self.torch.uint8, "workspace")
+        return self._ws
 
     def seq_tokens(self, b):
         if b not in self.tokens:
@@ -89,14 +141,15 @@ class GpuRun:
         ckv, kr, q = self.step_inputs(s)
         pos = (self.lens - 1 + s).astype(np.int32)
         lens_now = (self.lens + s).astype(np.int32)
-        lse_t = (torch.empty(self.w.batch, self.w.heads, dtype=torch.float32, device=self.dev)
-                 if lse else None)
+        lse_t = self.lse if lse else None
+        ws = self.workspace([int(x) for x in lens_now])
         if fused:
             out = self.cache.write_decode(
                 to_dev(ckv, torch.bfloat16, self.dev), to_dev(kr, torch.bfloat16, self.dev),
                 to_dev(q, torch.bfloat16, self.dev), to_dev(lens_now, torch.int32, self.dev),
-                lens_now, self.w.softmax_scale, lse=lse_t)
+                lens_now, self.w.softmax_scale, out=self.out, lse=lse_t, workspace=ws)
             torch.cuda.synchronize()
+            self.guards.check()
             self.step = s
             return out.cpu().numpy(), (lse_t.cpu().numpy() if lse else None)
         self.cache.write(to_dev(ckv, torch.bfloat16, self.dev), to_dev(kr, torch.bfloat16, self.dev),
@@ -104,8 +157,9 @@ class GpuRun:
                          seq_lens_after=to_dev(lens_now, torch.int32, self.dev))
         out = self.cache.decode(to_dev(q, torch.bfloat16, self.dev),
                                 to_dev(lens_now, torch.int32, self.dev), lens_now,
-                                self.w.softmax_scale, lse=lse_t)
+                                self.w.softmax_scale, out=self.out, lse=lse_t, workspace=ws)
         torch.cuda.synchronize()
+        self.guards.check()
         self.step = s
         return out.cpu().numpy(), (lse_t.cpu().numpy() if lse else None)
 

@@ -168,9 +168,21 @@ def test_full_v3_sampled_sequences():
     _full("v3_c4r4", seqs=[0, 13, 31])
 
 
-@pytest.mark.parametrize("name", ["long_c4r4", "long_bf16", "long16_c4r4"])
+@pytest.mark.parametrize("name", ["long_c4r4", "long_bf16", "long16_c4r4", "long16_bf16"])
 def test_full_long_context_sampled(name):
     _full(name, seqs=[2])
+
+
+@pytest.mark.parametrize("cb", [4, 2])
+def test_quarter_million_tokens(cb):
+    # past the 128K configurations: 262,144 cached tokens in one sequence (4,096
+    # pages, the most splits per sequence the planner makes for 16 heads);
+    # writer bytes bit-exact over the whole pool, decode within the bar, error
+    # word 0, guard bytes intact
+    w = syn.custom(f"q262k_c{cb}", [262144], heads=16, content_bits=cb, rope_bits=4, seed=37)
+    run = GpuRun(w)
+    run.prefill(keep_tokens=True)
+    _check_run_step(run, 0, lse=True)
 
 
 def test_full_mixed_c2r4_sixteen_steps():
