@@ -1,10 +1,15 @@
-"""Benchmark: low-bit MLA decode step on one GB300 (or N replicas under torchrun).
+"""Benchmark: low-bit MLA decode step on one GB300 (or N sequence shards under
+torchrun).
 
-One step = the fused cache writer appending one token per sequence, then the
-split-KV decode (+ log-sum-exp combine) over the whole cache, on the
-DeepSeek-V2-Lite-shaped C4R4 workload (8 sequences x 32768 tokens, 16 heads,
-latent 512 + rope 64, 64-token pages in random physical order) unless
-``--workload`` names another.  Inputs are synthetic and seeded (workloads/).
+One step = the split-KV decode (+ log-sum-exp combine) over the whole cache of
+the long-context C4R4 workload: 4 sequences x 131072 tokens, 128 heads sharing
+one latent (512) + RoPE (64) cache, 64-token pages in random physical order
+(the 128K configuration of the low-bit MLA decode benchmarks), unless
+``--workload`` names another; workloads with the writer in the step append one
+token per sequence first.  The same line reports, under ``configs``, the same
+step on bf16 pages, with 16 heads, and on the 32K DeepSeek-V2-Lite shape.
+Inputs are synthetic and seeded (workloads/).  Under torchrun each rank decodes
+its own shard of a global batch (world x batch sequences), no collective.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
 reference arm; bounded sample of the same workload).
@@ -263,6 +268,61 @@ def whole_job_tokens_per_s(world: int, batch: int, t_ms: float) -> float:
     return world * batch / (t_ms * 1e-3)
 
 
+def time_steps(s, step, passes: int, steps: int, warmup: int, stream, clk=None):
+    """Per-step device times (ms): ``passes`` independent passes, each with its own
+    warm-up, of ``steps`` timed steps; L2 is flushed (a write larger than L2)
+    before every step, outside the events."""
+    import torch
+    out = []
+    for p in range(passes):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if clk is not None and p == 0:
+            clk.mark(0)
+        for i in range(steps):
+            s.flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if clk is not None and p == passes - 1:
+            clk.mark(1)
+        out += [a_.elapsed_time(b_) for a_, b_ in ev]
+    return out
+
+
+def bytes_per_token(w: syn.Workload) -> int:
+    return {4: 324, 2: 196, 16: 1152}[w.content_bits]
+
+
+def config_record(w: syn.Workload, lens, ms, peak, tpk, kind: str):
+    """Measurements of one workload's decode step: times over all samples
+    (median, p10, p90, mean), throughput and the roofline fraction of the bound
+    that applies (tensor for packed caches read by 128 heads, else HBM)."""
+    mean = sum(ms) / len(ms)
+    by = algorithmic_bytes(w, lens)
+    step_bytes = by["decode"] + by["writer"]
+    gbs = step_bytes / (mean * 1e-3) / 1e9
+    tf = algorithmic_flops(w, lens) / (mean * 1e-3) / 1e12
+    tensor_bound = w.heads > 32 and w.content_bits != 16
+    rec = {"workload": w.name, "batch": w.batch, "heads": w.heads,
+           "layout": f"C{w.content_bits}R{w.rope_bits}" if w.content_bits != 16 else "bf16",
+           "context": int(lens[0]) if len(set(int(x) for x in lens)) == 1 else "mixed",
+           "writer_in_step": w.writer_in_step, "samples": len(ms),
+           "step_us": {"mean": round(mean * 1e3, 2),
+                       **{k: round(v * 1e3, 2) for k, v in percentiles(ms).items()}},
+           "tokens_per_s": round(w.batch / (mean * 1e-3), 1),
+           "kv_tokens_per_s": round(float(np.sum(lens)) / (mean * 1e-3), 1),
+           "bytes_per_token": bytes_per_token(w),
+           "packed_cache_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+           "tensor_tflops": round(tf, 2), "tensor_frac": round(tf / tpk, 4),
+           "bound": "tensor" if tensor_bound else "hbm", "kernel": kind}
+    return rec
+
+
 def run_gpu(args, w):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -274,80 +334,116 @@ def run_gpu(args, w):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = f"cuda:{local}"
     torch.cuda.set_device(local)
-    s = Setup(w, dev)
+    # this rank's shard of the global batch (world x the workload's batch):
+    # every sequence of the global batch is decoded by exactly one rank
+    ws_ = syn.shard_workload(w, rank, world)
+    s = Setup(ws_, dev)
     stream = torch.cuda.current_stream()
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
+    passes = 2
+    per_pass = max(1, args.steps // passes)
     clk = ClockSampler(local).__enter__()
-    for _ in range(args.warmup):
-        s.step()
-    torch.cuda.synchronize()
-
-    # ---- device-resident timed region: K steps, L2 flushed between them
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    clk.mark(0)
-    for i in range(args.steps):
-        s.flush.zero_()
-        ev[i][0].record(stream)
-        s.step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    clk.mark(1)
+    step_ms = time_steps(s, s.step, passes, per_pass, args.warmup, stream, clk)
     clk.__exit__(None, None, None)
     barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    dec_ms = step_ms  # the step is the (fused append +) decode call
 
     # ---- end to end through the public API with host buffers
+    e2e_steps = min(len(step_ms), 200)
     for _ in range(2):
         s.step_e2e()
     torch.cuda.synchronize()
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for i in range(args.steps):
+           for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
         s.flush.zero_()
         ev2[i][0].record(stream)
         s.step_e2e()
         ev2[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = [a.elapsed_time(b) for a, b in ev2]
+    e2e_ms = [a_.elapsed_time(b_) for a_, b_ in ev2]
     assert s.cache.error() == 0, f"device error word {s.cache.error()}"
+    assert bool(torch.isfinite(s.out).all()), "non-finite output"
 
     t_step = sum(step_ms) / len(step_ms)
-    t_dec = sum(dec_ms) / len(dec_ms)
     t_e2e = sum(e2e_ms) / len(e2e_ms)
-    t_step, t_dec, t_e2e = reduce_max_over_ranks([t_step, t_dec, t_e2e], dist, dev)
-    B = w.batch
+    t_step, t_e2e = reduce_max_over_ranks([t_step, t_e2e], dist, dev)
+    B = ws_.batch
     tokens_per_s = whole_job_tokens_per_s(world, B, t_step)
     e2e_tokens_per_s = whole_job_tokens_per_s(world, B, t_e2e)
-    by = algorithmic_bytes(w, s.lens)
     peak, peak_kind = peaks()
-    step_bytes = by["decode"] + by["writer"]
-    dec_gbs = step_bytes / (t_dec * 1e-3) / 1e9
-    tensor_bound = w.heads > 32 and w.content_bits != 16
     tpk, tpk_kind = tensor_peak()
-    dec_tflops = algorithmic_flops(w, s.lens) / (t_dec * 1e-3) / 1e12
-    trec = traffic_record(f"decode_{w.name}")
     # split + combine; the library fuses the append into the split kernel for
     # packed caches whose rows are not a multiple of 128 (the 128-row kernel
     # and bf16 pages run the writer kernel first)
     fused = w.writer_in_step and w.content_bits != 16 and w.heads % 128 != 0
     n_launch_step = 2 + (1 if w.writer_in_step and not fused else 0)
-    kernel_desc = ("append + decode (split kernel with fused append, combine)"
-                   if w.writer_in_step else "decode (split + combine)")
+    kernel_desc = ("append + decode (split kernel with fused append, combine)" if fused else
+                   "writer + decode (split + combine)" if w.writer_in_step else
+                   "decode (split + combine)")
+    head = config_record(ws_, s.lens, step_ms, peak, tpk, kernel_desc)
+    trec = traffic_record(f"decode_{w.name}")
+    by = algorithmic_bytes(ws_, s.lens)
+    step_bytes = by["decode"] + by["writer"]
+    dec_gbs = step_bytes / (t_step * 1e-3) / 1e9
+    dec_tflops = algorithmic_flops(ws_, s.lens) / (t_step * 1e-3) / 1e12
+    tensor_bound = head["bound"] == "tensor"
+    traffic = {"traffic": (trec or {}).get("dram_bytes_per_launch"),
+               "traffic_source": (f"ncu capture: {trec.get('profile')}" if trec else
+                                  "no ncu capture of the current kernel sources (null)")}
+    roofline = ({"bound": "tensor", "kernel": kernel_desc, "achieved": round(dec_tflops, 2),
+                 "peak": tpk, "peak_source": f"{tpk_kind} bf16_tflops (fp16 runs at the same rate)",
+                 "unit": "TFLOP/s", "frac": round(dec_tflops / tpk, 4),
+                 "algorithmic_flops": algorithmic_flops(ws_, s.lens),
+                 "hbm_frac": round(dec_gbs / peak, 4), **traffic}
+                if tensor_bound else
+                {"bound": "hbm", "kernel": kernel_desc, "achieved": round(dec_gbs, 1),
+                 "peak": peak, "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                 "frac": round(dec_gbs / peak, 4), "algorithmic_bytes": step_bytes, **traffic})
+
+    # ---- the other configurations of the same metric, one GPU (rank 0 alone)
+    configs = {}
+    if rank == 0 and world == 1 and not args.no_extra_configs:
+        del s
+        torch.cuda.empty_cache()
+        for name in EXTRA_CONFIGS.get(w.name, ()):
+            wx = syn.get(name)
+            sx = Setup(wx, dev)
+            fused_x = wx.writer_in_step and wx.content_bits != 16 and wx.heads % 128 != 0
+            ms = time_steps(sx, sx.step, passes, max(1, args.extra_steps // passes),
+                            args.warmup, stream)
+            assert sx.cache.error() == 0, f"device error word {sx.cache.error()} ({name})"
+            configs[name] = config_record(
+                wx, sx.lens, ms, peak, tpk,
+                ("append + decode" if fused_x else "writer + decode") if wx.writer_in_step
+                else "decode")
+            del sx
+            torch.cuda.empty_cache()
+        # the pages' comparison: packed against bf16 pages on the same values
+        for packed, plain in (("long_c4r4", "long_bf16"), ("long16_c4r4", "long16_bf16")):
+            recs = {**configs, w.name: head}
+            if packed in recs and plain in recs:
+                a_, b_ = recs[packed], recs[plain]
+                L = 131072
+                comp = (L * 1152) / ((L - 132) * 324 + 132 * 1152)
+                configs[f"{packed}_vs_{plain}"] = {
+                    "speedup": round(b_["step_us"]["mean"] / a_["step_us"]["mean"], 3),
+                    "delta_pct_table9": round(100.0 * (a_["step_us"]["mean"] / b_["step_us"]["mean"] - 1), 1),
+                    "bytes_per_token": [324, 1152],
+                    "compression_closed_form_at_128k": round(comp, 3)}
+
     if rank == 0:
         line = {
             "metric": METRIC,
             "value": round(tokens_per_s, 1),
             "unit": "tokens/s",
             "n_gpus": world,
-            "steps": args.steps,
+            "steps": len(step_ms),
             "warmup": args.warmup,
             "ms_per_step": round(t_step, 5),
             "higher_is_better": True,
@@ -355,37 +451,27 @@ def run_gpu(args, w):
             "vs_baseline": None,
             "dtype": "f16-mma/f32 (int codes exact)",
             "data": "synthetic (seeded; workloads/synthetic.py)",
-            "config": {"workload": w.name, "batch_per_gpu": B, "heads": w.heads,
-                       "context": [int(x) for x in s.lens][:8],
-                       "layout": f"C{w.content_bits}R{w.rope_bits}" if w.content_bits != 16
-                       else "bf16", "page_tokens": 64, "writer_in_step": w.writer_in_step,
-                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
-                       "parallelism": f"replicas x{world}"},
+            "config": {"workload": w.name, "batch_per_gpu": B, "global_batch": B * world,
+                       "heads": w.heads, "context": [int(x) for x in s_lens(ws_)][:8],
+                       "layout": head["layout"], "page_tokens": 64,
+                       "writer_in_step": w.writer_in_step,
+                       "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                       "sampling": f"{passes} independent passes x {per_pass} steps, each pass "
+                                   f"after its own {args.warmup} warm-up steps",
+                       "parallelism": f"sequence shards x{world} (no collective)"},
             "packed_cache_gbs": round(dec_gbs, 1),
             "hbm_frac": round(dec_gbs / peak, 4),
-            "decode_us": round(t_dec * 1e3, 2),
-            "kv_tokens_per_s": round(world * float(np.sum(s.lens)) / (t_step * 1e-3), 1),
-            "roofline": ({"bound": "tensor", "kernel": kernel_desc,
-                          "achieved": round(dec_tflops, 2), "peak": tpk,
-                          "peak_source": f"{tpk_kind} bf16_tflops (fp16 runs at the same rate)",
-                          "unit": "TFLOP/s", "frac": round(dec_tflops / tpk, 4),
-                          "algorithmic_flops": algorithmic_flops(w, s.lens),
-                          "hbm_frac": round(dec_gbs / peak, 4),
-                          "traffic": (trec or {}).get("dram_bytes_per_launch")}
-                         if tensor_bound else
-                         {"bound": "hbm", "kernel": kernel_desc,
-                          "achieved": round(dec_gbs, 1), "peak": peak,
-                          "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
-                          "frac": round(dec_gbs / peak, 4),
-                          "algorithmic_bytes": step_bytes,
-                          "traffic": (trec or {}).get("dram_bytes_per_launch")}),
-            "step_ms_percentiles": percentiles(step_ms),
-            "decode_us_percentiles": {k: round(v * 1e3, 2) for k, v in percentiles(dec_ms).items()},
+            "tensor_frac": round(dec_tflops / tpk, 4),
+            "decode_us": round(t_step * 1e3, 2),
+            "kv_tokens_per_s": round(world * float(np.sum(s_lens(ws_))) / (t_step * 1e-3), 1),
+            "roofline": roofline,
+            "step_us_percentiles": head["step_us"],
             "e2e": {"value": round(e2e_tokens_per_s, 1), "unit": "tokens/s",
-                    "h2d_bytes_per_step": int(s.n_in * 2),
-                    "d2h_bytes_per_step": int(s.h_out.numel() * 4)},
-            "gpu_launches": n_launch_step * args.steps,
+                    "h2d_bytes_per_step": int(e2e_in_bytes(ws_)),
+                    "d2h_bytes_per_step": int(ws_.batch * ws_.heads * 512 * 4)},
+            "gpu_launches": n_launch_step * len(step_ms),
             "clocks": clk.summary(),
+            "configs": configs,
         }
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
@@ -394,7 +480,34 @@ def run_gpu(args, w):
         dist.destroy_process_group()
 
 
+# the other workloads reported beside a headline workload (one GPU)
+EXTRA_CONFIGS = {
+    "long_c4r4": ("long_bf16", "long16_c4r4", "long16_bf16", "v2lite_c4r4"),
+    "long16_c4r4": ("long16_bf16",),
+    "v2lite_c4r4": (),
+}
+
+
+def s_lens(w: syn.Workload):
+    return syn.sequence_lengths(w)
+
+
+def e2e_in_bytes(w: syn.Workload) -> int:
+    """Host-to-device bytes of one end-to-end step: q, plus the new tokens when
+    the writer is in the step."""
+    n = w.batch * w.heads * 576
+    if w.writer_in_step:
+        n += w.batch * (512 + 64)
+    return 2 * n
+
+
 # ---------------------------------------------------------------- the oracle arm
+
+# heads of sequence 0 that one oracle step decodes (a bounded sample of the
+# workload's step); the step counts as ORACLE_HEADS / heads of an output token
+ORACLE_HEADS = 16
+REFERENCE_SECONDS = 150.0   # cap on the reference arm's timed region
+
 
 def _oracle_sample(w: syn.Workload):
     """Oracle state for sequence 0 of the workload (prefilled, not timed)."""
@@ -409,7 +522,7 @@ def _oracle_sample(w: syn.Workload):
     lens_after = np.zeros(w.batch, np.int64)
     lens_after[b] = L - 1
     model.write(np.full(L - 1, b), np.arange(L - 1), ckv[:L - 1], kr[:L - 1], lens_after)
-    q = syn.queries(w, b)[0]
+    q = syn.queries(w, b)[0][:ORACLE_HEADS]
     return model, b, L, ckv[L - 1:L], kr[L - 1:L], q
 
 
@@ -422,10 +535,19 @@ def _oracle_step(w, model, b, L, ckv1, kr1, q):
     return oracle.mla_decode_fp64(q, model.effective_keys(b, L), w.softmax_scale)
 
 
+def _sample_text(w, n, L, el):
+    nh = min(ORACLE_HEADS, w.heads)
+    return (f"{n} oracle steps of sequence 0 (L={L}, {nh} of {w.heads} heads per step = "
+            f"{nh / w.heads:g} output token{', writer + ' if w.writer_in_step else ', '}"
+            f"fp64 attention) of {w.name}, {el:.1f} s")
+
+
 def cpu_baseline(w: syn.Workload, budget_s: float):
-    """The oracle as it stands, timed on this host for one sequence per step,
-    repeated until ``budget_s`` seconds; tokens/s = output tokens / time."""
+    """The oracle as it stands, timed on this host for a bounded sample of the
+    workload's step, repeated until ``budget_s`` seconds; tokens/s = output
+    tokens (the sampled fraction of each) / time."""
     model, b, L, ckv1, kr1, q = _oracle_sample(w)
+    frac = min(ORACLE_HEADS, w.heads) / w.heads
     n, t0 = 0, time.perf_counter()
     while True:
         _oracle_step(w, model, b, L, ckv1, kr1, q)
@@ -433,11 +555,8 @@ def cpu_baseline(w: syn.Workload, budget_s: float):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": round(n / el, 4), "unit": "tokens/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{n} decode steps of sequence 0 (L={L}, {w.heads} heads"
-                      f"{', writer + ' if w.writer_in_step else ', '}fp64 attention) of "
-                      f"{w.name}, {el:.1f} s"}
+    return {"value": round(n * frac / el, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": _sample_text(w, n, L, el)}
 
 
 def run_reference(args, w):
@@ -445,25 +564,29 @@ def run_reference(args, w):
     if rank != 0:
         return
     model, b, L, ckv1, kr1, q = _oracle_sample(w)
-    for _ in range(max(args.warmup, 0)):
+    frac = min(ORACLE_HEADS, w.heads) / w.heads
+    for _ in range(min(max(args.warmup, 0), 1)):
         _oracle_step(w, model, b, L, ckv1, kr1, q)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
+    n, t0 = 0, time.perf_counter()
+    while n < args.steps:
         _oracle_step(w, model, b, L, ckv1, kr1, q)
+        n += 1
+        if time.perf_counter() - t0 > REFERENCE_SECONDS:
+            break
     el = time.perf_counter() - t0
-    value = args.steps / el
+    value = n * frac / el
     world = int(os.environ.get("WORLD_SIZE", "1"))
     line = {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(el / n * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; workloads/synthetic.py)",
         "config": {"workload": w.name, "batch_per_gpu": w.batch, "heads": w.heads,
-                   "sample": "sequence 0 per step (CPU oracle)"},
+                   "sample": f"sequence 0, {min(ORACLE_HEADS, w.heads)} heads per step "
+                             f"(CPU oracle; at most {REFERENCE_SECONDS:.0f} s of steps)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(),
-                         "kind": "oracle",
-                         "sample": f"{args.steps} decode steps of sequence 0 (L={L})"},
+                         "kind": "oracle", "sample": _sample_text(w, n, L, el)},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -632,10 +755,14 @@ def run_rotate(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=600,
+                    help="timed steps of the headline workload, in two independent passes")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--extra-steps", type=int, default=120,
+                    help="timed steps of each other configuration in the line")
+    ap.add_argument("--no-extra-configs", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="v2lite_c4r4", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--workload", default="long_c4r4", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", choices=["table9", "mtp", "rotate"], default=None,

@@ -1,7 +1,8 @@
-"""The replica path of bench.py with two ranks on CPU (gloo): the decode path
-shards by sequence with no data-path collective, so N GPUs run N replicas and
-the only communication is the barrier and the max over ranks of the step
-times.  Whole-job throughput counts the tokens of every rank."""
+"""The multi-GPU path of bench.py with two ranks on CPU (gloo): the decode
+shards a seeded global batch by sequence (global sequence g on rank g mod N)
+with no data-path collective; the only communication is the barrier and the
+max over ranks of the step times.  Whole-job throughput counts the tokens of
+every rank."""
 
 import os
 import socket
@@ -73,3 +74,84 @@ def test_reference_arm_runs_on_rank_zero_only():
     line = json.loads(outs[0].strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert outs[1].strip() == ""             # the other rank exits without work or output
+
+
+def test_sequence_shards_cover_the_global_batch_once():
+    # Each rank builds only its sequences' lengths, pages and block table; the
+    # union over ranks is the global batch exactly once, each shard carries the
+    # global values of its sequences, and the oracle's outputs of the shards,
+    # put back in global order, are the single-rank result.
+    outs = _run_ranks("""
+        import json
+        import numpy as np
+        import torch
+        import torch.distributed as dist
+        import oracle
+        from workloads import synthetic as syn
+        dist.init_process_group("gloo")
+        r, n = dist.get_rank(), dist.get_world_size()
+        w = syn.get("tiny_c4r4").with_(name="tiny_u", batch=3, length_kind="uniform",
+                                        length_args=(140, 400), seed=17)
+        sh = syn.shard_workload(w, r, n)
+        glob = w.with_(batch=w.batch * n)
+        ids = list(sh.seq_ids)
+        # every rank's ids, gathered
+        allids = [None] * n
+        dist.all_gather_object(allids, ids)
+        # this shard against the global draw: lengths and token values
+        gl = syn.sequence_lengths(glob)
+        lens = syn.sequence_lengths(sh)
+        assert [int(x) for x in lens] == [int(gl[g]) for g in ids]
+        table, npages = syn.make_paging(sh)
+        assert table.shape[0] == len(ids) and table.max() < npages
+        for b, g in enumerate(ids):
+            t_s, k_s = syn.sequence_tokens(sh, b)
+            t_g, k_g = syn.sequence_tokens(glob, g)
+            assert np.array_equal(t_s, t_g) and np.array_equal(k_s, k_g)
+            assert np.array_equal(syn.queries(sh, b), syn.queries(glob, g))
+        # the oracle decode of every shard sequence on this rank's own cache
+        model = oracle.PagedCacheModel(oracle.Layout(4, 4), npages, table)
+        outs = {}
+        for b, g in enumerate(ids):
+            L = int(lens[b])
+            ckv, kr = syn.sequence_tokens(sh, b)
+            la = np.zeros(len(ids), np.int64)
+            la[b] = L
+            model.write(np.full(L, b), np.arange(L), ckv, kr, la)
+            o, _ = oracle.mla_decode_fp64(syn.queries(sh, b)[0], model.effective_keys(b, L),
+                                          w.softmax_scale)
+            outs[g] = o.tolist()
+        gathered = [None] * n
+        dist.all_gather_object(gathered, outs)
+        if r == 0:
+            merged = {}
+            for d in gathered:
+                merged.update({int(k): v for k, v in d.items()})
+            print(json.dumps({"ids": allids, "outs": merged}))
+        dist.destroy_process_group()
+    """, timeout=300)
+    import json
+
+    import numpy as np
+
+    import oracle
+    from workloads import synthetic as syn
+    res = json.loads(outs[0].strip().splitlines()[-1])
+    flat = [g for ids in res["ids"] for g in ids]
+    assert sorted(flat) == list(range(6)) and len(flat) == len(set(flat))   # once each
+    assert res["ids"] == [[0, 2, 4], [1, 3, 5]]                              # g mod N
+    # single-rank reference: the global batch on one cache
+    w = syn.get("tiny_c4r4").with_(name="tiny_u", batch=6, length_kind="uniform",
+                                    length_args=(140, 400), seed=17)
+    table, npages = syn.make_paging(w)
+    model = oracle.PagedCacheModel(oracle.Layout(4, 4), npages, table)
+    lens = syn.sequence_lengths(w)
+    for g in range(6):
+        L = int(lens[g])
+        ckv, kr = syn.sequence_tokens(w, g)
+        la = np.zeros(6, np.int64)
+        la[g] = L
+        model.write(np.full(L, g), np.arange(L), ckv, kr, la)
+        ref, _ = oracle.mla_decode_fp64(syn.queries(w, g)[0], model.effective_keys(g, L),
+                                        w.softmax_scale)
+        assert np.array_equal(np.asarray(res["outs"][str(g)]), ref)

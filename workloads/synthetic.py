@@ -68,6 +68,11 @@ class Workload:
     seed: int = 0
     writer_in_step: bool = False  # the timed step also runs the cache writer
     softmax_scale: float = 1.0 / math.sqrt(192.0)
+    # Global indices of this workload's sequences in the batch they were drawn
+    # from (a rank's shard); None means sequence b is global sequence b.  Token
+    # and query draws follow the global index, so a shard holds exactly the
+    # values its sequences have in the global batch.
+    seq_ids: Optional[Tuple[int, ...]] = None
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -161,7 +166,8 @@ def make_paging(w: Workload, spare_pages: int = 0):
 
 
 def _seq_streams(w: Workload, b: int):
-    return _children(w)[3 + b].spawn(2)
+    g = b if w.seq_ids is None else int(w.seq_ids[b])
+    return np.random.SeedSequence(w.seed).spawn(3 + g + 1)[3 + g].spawn(2)
 
 
 def sequence_tokens(w: Workload, b: int, n_tokens: Optional[int] = None,
@@ -201,6 +207,24 @@ def queries(w: Workload, b: int) -> np.ndarray:
     rng = np.random.default_rng(_seq_streams(w, b)[1])
     q = rng.standard_normal((w.steps, w.heads, QK_DIM), dtype=np.float32)
     return bf16_bits_from_f32(q)
+
+
+def shard_workload(w: Workload, rank: int, world: int) -> Workload:
+    """Rank ``rank``'s shard of the global batch of ``world * w.batch`` sequences
+    drawn from ``w``'s recipe: global sequence g goes to rank g mod world, so
+    every sequence is decoded by exactly one rank and ranks share nothing (no
+    data-path exchange).  The shard keeps the global lengths and values of its
+    sequences; its page pool and block table are its own.  With world == 1 the
+    shard is ``w`` itself (same lengths, values and paging)."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"rank {rank} of {world}")
+    glob = w.with_(batch=w.batch * world)
+    if world > 1 and w.length_kind == "explicit":
+        raise ValueError("explicit lengths name one batch; shard a recipe workload")
+    lens = sequence_lengths(glob)
+    ids = tuple(g for g in range(glob.batch) if g % world == rank)
+    return w.with_(batch=len(ids), length_kind="explicit",
+                   length_args=tuple(int(lens[g]) for g in ids), seq_ids=ids)
 
 
 def custom(name: str, lengths: Sequence[int], heads: int = 16, content_bits: int = 4,
