@@ -47,19 +47,28 @@ __device__ __forceinline__ void bar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One test of an mbarrier phase (no suspension).
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase; on time-out raises the CTA abort flag.
+// A phase that is already complete costs one test: the clock and the abort
+// flag are read only when the thread has to wait (reading the clock behind
+// outstanding tensor-core work costs a few hundred cycles).
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                          int32_t* err, long long limit = kWaitCycles) {
+  if (bar_test(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
+    if (bar_test(bar, parity)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
       *abort = 1;
@@ -235,7 +244,7 @@ __device__ __forceinline__ void arrive_peer_relaxed(uint32_t bar_cluster_addr) {
 // Bounded wait for arrivals from the peer that carry no data.
 __device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
                                                  int32_t* err, long long limit = kWaitCycles) {
-  const long long t0 = clock64();
+  long long t0 = -1;
   for (;;) {
     uint32_t ok;
     asm volatile(
@@ -246,6 +255,7 @@ __device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity, 
         : "memory");
     if (ok) return true;
     if (*abort) return false;
+    if (t0 < 0) t0 = clock64();
     if (clock64() - t0 > limit) {
       *abort = 1;
       set_error(err, MLA_LOWBIT_DEV_PIPELINE);
@@ -259,6 +269,7 @@ __device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity, 
 constexpr uint32_t kSuspendNs = 200000;
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* err,
                                      long long limit = kWaitCycles) {
+  if (bar_test(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     uint32_t ok;
