@@ -35,13 +35,15 @@
 //   (128 x 256 fp32) stays in tensor memory for the whole split and is
 //   rescaled only when a row's running max grows by more than kLazy.
 //
-// Warp roles (416 threads, one CTA per SM):
+// Warp roles (448 threads, one CTA per SM):
 //   warps 0-3   unpack: two threads per token of the tile (one per half of the
 //               CTA's groups); the next tile's bytes are loaded into registers
 //               while a plane buffer drains;
 //   warps 4-11  softmax: TMEM lane quadrant w & 3 (32 rows), token half
 //               (w - 4) >> 2 (32 tokens);
-//   warp 12     MMA issue (one lane) and the TMEM allocation.
+//   warp 12     QK issue (one lane) and the TMEM allocation;
+//   warp 13     PV issue (one lane): a tile's PV starts as soon as its P is in
+//               tensor memory, whatever the next tile's QK is waiting for.
 // Every wait is bounded; on a time-out the CTA records MLA_LOWBIT_DEV_PIPELINE,
 // the softmax warps of a quadrant leave the tile loop together, the partial is
 // written empty, and tensor memory is still freed.
@@ -54,11 +56,12 @@ namespace wide {
 using namespace tc;
 
 constexpr int kRows = 128;
-constexpr int kThreads = 416;
+constexpr int kThreads = 448;
 constexpr int kUnpackThreads = 128;
 constexpr int kSoftWarp0 = 4;
 constexpr int kSoftThreads = 256;
-constexpr int kIssuerWarp = 12;
+constexpr int kIssuerWarp = 12;      // QK
+constexpr int kPvWarp = 13;          // PV
 constexpr int kTW = 32;                 // tokens of a tile per softmax warp
 constexpr int kNB = 2;                  // plane-set ring depth (tiles)
 constexpr int kMaxOwn = 5;              // QK groups of a CTA
@@ -95,7 +98,7 @@ constexpr int kBarDFull = 4;    // count 1: the tile's QK is complete
 constexpr int kBarDFree = 5;    // count 256: the softmax warps have read it
 constexpr int kBarPFull = 6;    // count 256: P of the tile is in tensor memory
 constexpr int kBarPFree = 7;    // count 1: the tile's PV is complete
-constexpr int kBarFlush = 8;    // count 1: final drain of the issuer
+constexpr int kBarFlush = 8;    // count 2: final drain of both issuers
 constexpr int kBarXFull = 9;    // [8] per softmax warp w: count 1 + 4 KB of transactions, the peer's
                                 //     warp w has written its partial logits into my buffer
 constexpr int kBarXFree = 17;   // [8] per softmax warp w: count 1, the peer's warp w has read its buffer
@@ -284,7 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::bar_init(bar(kBarXFull + w), 1);
       tc::bar_init(bar(kBarXFree + w), 1);
     }
-    tc::bar_init(bar(kBarFlush), 1);
+    tc::bar_init(bar(kBarFlush), 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -423,35 +426,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) cc[k] = nc[k];
       const uint2 rr = nr;
-      uint32_t mw[3] = {nm[0], nm[1], nm[2]};
+      const uint32_t mw0 = nm[0], mw1 = nm[1], mw2 = nm[2];
       const bool okt_cur = n_okt;
       if (i + 1 < n_pk) fetch(i + 1);  // in flight while the buffer drains
-      if (i >= kNB && !wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err, a.wait_cycles)) break;
-      uint8_t* A = sA + buf * kABuf;
-      float* meta = sMeta + buf * kMaxOwn * 64;
-      bool okt, shifted = false;
-      if (i < n_pk) {
-        okt = okt_cur;
+      const bool packed = i < n_pk;
+      // What needs only this tile's metadata is done before the buffer is
+      // free: the token factor, the scale parts, m', the min-term chunks, the
+      // RoPE codes and the validity mask.
+      bool shift = false;
+      uint32_t hiA = 0u, loA = 0u, hiB = 0u, loB = 0u, hiR = 0u, loR = 0u;
+      float mqA = 0.f, mqB = 0.f;  // m' of the two content groups, in order
+      uint32_t rc[8];              // the two RoPE words' centred codes
+      uint4 mc0 = make_uint4(0, 0, 0, 0), mc1 = mc0;
+      if (packed) {
         // one factor per token: 2^-4 on both planes when some group's s * |c|
         // could leave the fp16 range (decided with the token's other half)
         float smax = 0.f;
+        const uint32_t mws[3] = {mw0, mw1, mw2};
 #pragma unroll
         for (int jj = 0; jj < 3; ++jj) {
-          const float s = __half2float(__ushort_as_half((unsigned short)(mw[jj] & 0xFFFFu)));
-          smax = fmaxf(smax, s * (jj < 2 ? kCmaxC : 8.f));
+          const float sv = __half2float(__ushort_as_half((unsigned short)(mws[jj] & 0xFFFFu)));
+          smax = fmaxf(smax, sv * (jj < 2 ? kCmaxC : 8.f));
         }
         smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
-        const bool shift = smax > kShiftAbove;
-        shifted = shift;
+        shift = smax > kShiftAbove;
+        scale_parts(mw0 & 0xFFFFu, shift, hiA, loA);
+        scale_parts(mw1 & 0xFFFFu, shift, hiB, loB);
+        scale_parts(mw2 & 0xFFFFu, shift, hiR, loR);
+        const float2 smA = __half22float2(*reinterpret_cast<const __half2*>(&mw0));
+        const float2 smB = __half22float2(*reinterpret_cast<const __half2*>(&mw1));
+        mqA = fmaf(kCentreC, smA.x, smA.y);
+        mqB = fmaf(kCentreC, smB.x, smB.y);
+        unpack_int4(rr.x, rc);
+        unpack_int4(rr.y, rc + 4);
+        // min-term k-steps of the token (B side): m' of the CTA's content
+        // groups (two from each thread of the token) and, on rank 1, of the
+        // RoPE group, times the token's plane factor; thread gh writes the
+        // chunks of k-step X (gh = 0) or Y (gh = 1)
+        const float2 smr = __half22float2(*reinterpret_cast<const __half2*>(&mw2));
+        const float pa = __shfl_xor_sync(0xffffffffu, mqA, 1);
+        const float pb = __shfl_xor_sync(0xffffffffu, mqB, 1);
+        const float f = shift ? 0.0625f : 1.f;
+        const float mv[kMaxOwn] = {gh ? pa : mqA, gh ? pb : mqB, gh ? mqA : pa, gh ? mqB : pb,
+                                   r ? fmaf(float(kCentre4), smr.x, smr.y) : 0.f};
+        float mh[kMaxOwn], mm[kMaxOwn], ml[kMaxOwn];
+#pragma unroll
+        for (int j = 0; j < kMaxOwn; ++j) split3_bf16(mv[j] * f, mh[j], mm[j], ml[j]);
+        mc0 = min_chunk_b(2 * gh, mh, mm, ml);
+        mc1 = min_chunk_b(2 * gh + 1, mh, mm, ml);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rc[k] = 0u;
+      }
+      const bool okt = packed ? okt_cur : bf_first + (i - n_pk) * 64 + t < bf_end;
+      // validity of the warp's 16 tokens (lanes 2k and 2k+1 hold token k);
+      // bit 31: some token of the 16 has its planes scaled by 2^-4
+      const bool any_shift = __any_sync(0xffffffffu, shift);
+      uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
+      mk = (mk | (mk >> 1)) & 0x33333333u;
+      mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
+      mk = (mk | (mk >> 4)) & 0x00FF00FFu;
+      mk = (mk | (mk >> 8)) & 0x0000FFFFu;
+      // the buffer: free once the PV of tile i - kNB is complete (the lanes of
+      // a warp leave together)
+      const bool free_ok = i < kNB || wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err, a.wait_cycles);
+      if (!__all_sync(0xffffffffu, free_ok)) break;
+      uint8_t* A = sA + buf * kABuf;
+      float* meta = sMeta + buf * kMaxOwn * 64;
+      if (packed) {
         if (gh == 0) sShift[buf * 64 + t] = shift ? 16.f : 1.f;
         // the thread's two content groups in a rolled loop (code size): the
-        // group in hand is always cc[0..], mw[0], shifted down afterwards
-        float mq0 = 0.f, mq1 = 0.f;  // m' of the two groups, in order
+        // group in hand is always cc[0..] with hiA/loA/mqA, shifted down afterwards
 #pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * gh + jj;
-          uint32_t hi2, lo2;
-          scale_parts(mw[0] & 0xFFFFu, shift, hi2, lo2);
           uint8_t* p1 = A + j * kPlane;
           uint8_t* p2 = A + (kMaxOwn + j) * kPlane;
           // the token's two threads write the same positions of planes 8 KB
@@ -466,9 +514,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               uint32_t p[4];
               unpack_int4(gh ? w[k2 ^ 4] : w[k2], p);
               *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, kk)) =
-                  make_uint4(hmul2u(p[0], hi2), hmul2u(p[1], hi2), hmul2u(p[2], hi2), hmul2u(p[3], hi2));
+                  make_uint4(hmul2u(p[0], hiA), hmul2u(p[1], hiA), hmul2u(p[2], hiA), hmul2u(p[3], hiA));
               *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, kk)) =
-                  make_uint4(hmul2u(p[0], lo2), hmul2u(p[1], lo2), hmul2u(p[2], lo2), hmul2u(p[3], lo2));
+                  make_uint4(hmul2u(p[0], loA), hmul2u(p[1], loA), hmul2u(p[2], loA), hmul2u(p[3], loA));
             }
           } else {
             const uint4 c0 = cc[0];
@@ -481,69 +529,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 2 * kk + hh)) =
-                    make_uint4(hmul2u(p[4 * hh], hi2), hmul2u(p[4 * hh + 1], hi2),
-                               hmul2u(p[4 * hh + 2], hi2), hmul2u(p[4 * hh + 3], hi2));
+                    make_uint4(hmul2u(p[4 * hh], hiA), hmul2u(p[4 * hh + 1], hiA),
+                               hmul2u(p[4 * hh + 2], hiA), hmul2u(p[4 * hh + 3], hiA));
                 *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, 2 * kk + hh)) =
-                    make_uint4(hmul2u(p[4 * hh], lo2), hmul2u(p[4 * hh + 1], lo2),
-                               hmul2u(p[4 * hh + 2], lo2), hmul2u(p[4 * hh + 3], lo2));
+                    make_uint4(hmul2u(p[4 * hh], loA), hmul2u(p[4 * hh + 1], loA),
+                               hmul2u(p[4 * hh + 2], loA), hmul2u(p[4 * hh + 3], loA));
               }
             }
           }
-          const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(&mw[0]));
-          const float mq = fmaf(kCentreC, sm.x, sm.y);
-          meta[j * 64 + t] = mq;
-          mq0 = mq1;
-          mq1 = mq;
+          meta[j * 64 + t] = mqA;
+          mqA = mqB;
+          hiA = hiB;
+          loA = loB;
           if constexpr (CB == 4) {
             cc[0] = cc[2];
             cc[1] = cc[3];
           } else {
             cc[0] = cc[1];
           }
-          mw[0] = mw[1];
         }
         {
           // RoPE words 4r + 2gh, 4r + 2gh + 1 -> chunks of the same index
-          uint32_t hi2, lo2;
-          scale_parts(mw[2] & 0xFFFFu, shift, hi2, lo2);
           uint8_t* p1 = A + 4 * kPlane;
           uint8_t* p2 = A + (kMaxOwn + 4) * kPlane;
-          const uint32_t w[2] = {rr.x, rr.y};
 #pragma unroll
           for (int k2 = 0; k2 < 2; ++k2) {
             const int c = 4 * r + 2 * gh + k2;
-            uint32_t p[4];
-            unpack_int4(w[k2], p);
+            const uint32_t* p = rc + 4 * k2;
             *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, c)) =
-                make_uint4(hmul2u(p[0], hi2), hmul2u(p[1], hi2), hmul2u(p[2], hi2), hmul2u(p[3], hi2));
+                make_uint4(hmul2u(p[0], hiR), hmul2u(p[1], hiR), hmul2u(p[2], hiR), hmul2u(p[3], hiR));
             *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, c)) =
-                make_uint4(hmul2u(p[0], lo2), hmul2u(p[1], lo2), hmul2u(p[2], lo2), hmul2u(p[3], lo2));
+                make_uint4(hmul2u(p[0], loR), hmul2u(p[1], loR), hmul2u(p[2], loR), hmul2u(p[3], loR));
           }
-        }
-        {
-          // min-term k-steps of the token (B side): m' of the CTA's content
-          // groups (two from each thread of the token) and, on rank 1, of the
-          // RoPE group, times the token's plane factor; thread gh writes the
-          // chunks of k-step X (gh = 0) or Y (gh = 1)
-          const float2 smr = __half22float2(*reinterpret_cast<const __half2*>(&mw[2]));
-          const float pa = __shfl_xor_sync(0xffffffffu, mq0, 1);
-          const float pb = __shfl_xor_sync(0xffffffffu, mq1, 1);
-          const float f = shift ? 0.0625f : 1.f;
-          const float mv[kMaxOwn] = {gh ? pa : mq0, gh ? pb : mq1, gh ? mq0 : pa, gh ? mq1 : pb,
-                                     r ? fmaf(float(kCentre4), smr.x, smr.y) : 0.f};
-          float mh[kMaxOwn], mm[kMaxOwn], ml[kMaxOwn];
-#pragma unroll
-          for (int j = 0; j < kMaxOwn; ++j) split3_bf16(mv[j] * f, mh[j], mm[j], ml[j]);
-          uint8_t* p1 = A + 4 * kPlane;
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2)
-            *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
-                min_chunk_b(2 * gh + c2, mh, mm, ml);
+          *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh)) = mc0;
+          *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + 1)) = mc1;
         }
       } else {
         // protected tokens: bf16 values as the s_hi plane, zero s_lo plane, min 0
         const int idx = bf_first + (i - n_pk) * 64 + t;
-        okt = idx < bf_end;
         const uint16_t* rp = nullptr;
         if (okt) {
           const int pos = bf16_pos(sw, idx);
@@ -590,23 +613,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(A + 4 * kPlane + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
               make_uint4(0, 0, 0, 0);
       }
-      // validity of the warp's 16 tokens (lanes 2k and 2k+1 hold token k);
-      // bit 31: some token of the 16 has its planes scaled by 2^-4
-      const bool any_shift = __any_sync(0xffffffffu, shifted);
-      uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
-      mk = (mk | (mk >> 1)) & 0x33333333u;
-      mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
-      mk = (mk | (mk >> 4)) & 0x00FF00FFu;
-      mk = (mk | (mk >> 8)) & 0x0000FFFFu;
       if (lane == 0) sMask[buf * 4 + warp] = mk | (any_shift ? 0x80000000u : 0u);
       tc::fence_async_smem();
       // self-test of the bounded waits: the first tile's hand-off is withheld
       if (!(a.fault == 1 && i == 0)) tc::bar_arrive(bar(kBarAFull + buf));
     }
-  } else if (warp == kIssuerWarp) {
-    // ---------------- MMA issue (lane 0): the next tile's QK as soon as its
-    // planes are in and the softmax warps have read this tile's logits; then
-    // this tile's PV once P is in tensor memory
+  } else if (warp == kIssuerWarp || warp == kPvWarp) {
+    // ---------------- MMA issue (lane 0 of two warps): QK of each tile as soon
+    // as its planes are in and the softmax warps have read the previous tile's
+    // logits; PV of each tile once its P is in tensor memory.  Each issuer
+    // commits its own MMAs (a commit tracks the issuing thread's operations).
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc(128, 64, 0, 0);    // A K-major, B K-major
       // the same shape with bf16 A and B (bits 7-9, 10-12: format 1) for the
@@ -623,70 +639,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t kq0 = tc::desc(tc::su32(sA), 16, 1024);
       const uint64_t kp0 = tc::desc(tc::su32(sA), kPlane, 1024);
       const uint64_t qr0 = tc::desc(tc::su32(sQR), 16, 1024);
-      // (loops kept rolled: the issue rate is set by the tensor core, and the
-      // kernel's per-tile code has to stay small for the instruction caches)
-      auto issue_qk = [&](int i) {
-        const uint64_t d = kq0 + (uint64_t)(((i % kNB) * kABuf) >> 4);
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+      // (the issue loops are unrolled: with the descriptors folded to
+      // constants an MMA issues every ~46 cycles, against ~60 from a rolled loop)
+      if (warp == kIssuerWarp) {
+        for (int k = 0; k < n_tiles; ++k) {
+          if (!(tile_ready(k) && (k == 0 || wait(bar(kBarDFree), (k - 1) & 1, abort_flag, a.err, a.wait_cycles))))
+            break;
+          tc::tc_fence_after();
+          const uint64_t d = kq0 + (uint64_t)(((k % kNB) * kABuf) >> 4);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t qa = tmem + kColQ + 32 * j + 8 * ks;
+              mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, (j | ks) != 0);
+              mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
+            }
+          }
+          // this rank's half of the RoPE channels: k-steps 2r, 2r + 1
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int ks = 2 * r + k2;
+            tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                    d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_qk, 1);
+            tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                    d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
+          }
+          // the min terms: the other rank's RoPE k-steps, in bf16
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int ks = 2 * (1 - r) + k2;
+            tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                    d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+          }
+          tc::commit(bar(kBarDFull));
+        }
+      } else {
+        for (int k = 0; k < n_tiles; ++k) {
+          // P of tile k is in tensor memory; its planes were complete before
+          // its QK (tested again here: an acquire in this thread too)
+          if (!(wait(bar(kBarPFull), k & 1, abort_flag, a.err, a.wait_cycles) && tile_ready(k))) break;
+          tc::tc_fence_after();
+          const uint64_t d = kp0 + (uint64_t)(((k % kNB) * kABuf) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t qa = tmem + kColQ + 32 * j + 8 * ks;
-            mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, (j | ks) != 0);
-            mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
+            // the four content groups' planes side by side: N = 256 channels
+            const uint64_t b1 = d + (uint64_t)((2048 * ks) >> 4);
+            const uint64_t b2 = d + (uint64_t)((kMaxOwn * kPlane + 2048 * ks) >> 4);
+            const uint32_t phi = tmem + kColP + 8 * ks, plo = tmem + kColP + 32 + 8 * ks;
+            mma_tmem_a(tmem + kColO, phi, b1, id_pv, (k > 0 || ks > 0));
+            mma_tmem_a(tmem + kColO, plo, b1, id_pv, 1);
+            mma_tmem_a(tmem + kColO, phi, b2, id_pv, 1);
           }
-        }
-        // this rank's half of the RoPE channels: k-steps 2r, 2r + 1
-#pragma unroll 1
-        for (int k2 = 0; k2 < 2; ++k2) {
-          const int ks = 2 * r + k2;
-          tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                  d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_qk, 1);
-          tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                  d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
-        }
-        // the min terms: the other rank's RoPE k-steps, in bf16
-#pragma unroll 1
-        for (int k2 = 0; k2 < 2; ++k2) {
-          const int ks = 2 * (1 - r) + k2;
-          tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                  d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
-        }
-        tc::commit(bar(kBarDFull));
-      };
-      auto issue_pv = [&](int i) {
-        const uint64_t d = kp0 + (uint64_t)(((i % kNB) * kABuf) >> 4);
-#pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks) {
-          // the four content groups' planes side by side: N = 256 channels
-          const uint64_t b1 = d + (uint64_t)((2048 * ks) >> 4);
-          const uint64_t b2 = d + (uint64_t)((kMaxOwn * kPlane + 2048 * ks) >> 4);
-          const uint32_t phi = tmem + kColP + 8 * ks, plo = tmem + kColP + 32 + 8 * ks;
-          mma_tmem_a(tmem + kColO, phi, b1, id_pv, (i > 0 || ks > 0));
-          mma_tmem_a(tmem + kColO, plo, b1, id_pv, 1);
-          mma_tmem_a(tmem + kColO, phi, b2, id_pv, 1);
-        }
-        tc::commit(bar(kBarPFree));
-        tc::commit(bar(kBarAFree + i % kNB));
-      };
-      // step k: QK of tile k (once its planes are in and the softmax warps
-      // have read tile k-1's logits), then PV of tile k-1
-      bool ok = true;
-      for (int k = 0; ok && k <= n_tiles; ++k) {
-        if (k < n_tiles) {
-          ok = tile_ready(k) && (k == 0 || wait(bar(kBarDFree), (k - 1) & 1, abort_flag, a.err, a.wait_cycles));
-          if (!ok) break;
-          tc::tc_fence_after();
-          issue_qk(k);
-        }
-        if (k >= 1) {
-          ok = wait(bar(kBarPFull), (k - 1) & 1, abort_flag, a.err, a.wait_cycles);
-          if (!ok) break;
-          tc::tc_fence_after();
-          issue_pv(k - 1);
+          tc::commit(bar(kBarPFree));
+          tc::commit(bar(kBarAFree + k % kNB));
         }
       }
-      // drain (bounded, regardless of the abort flag) before TMEM is freed
+      // drain (bounded, regardless of the abort flag) before TMEM is freed:
+      // the barrier completes once both issuers' operations are done
       tc::commit(bar(kBarFlush));
       const long long t0 = clock64();
       for (;;) {
