@@ -70,6 +70,8 @@ constexpr int kABuf = 2 * kMaxOwn * kPlane;  // s_hi planes of the 5 groups, the
 constexpr int kQBlock = kRows * 128;    // 128 rows x 64 fp16
 constexpr float kLazy = 8.0f;           // log2 units
 constexpr float kShiftAbove = 32768.f;  // |s c| bound beyond which a token's planes are scaled by 2^-4
+constexpr int kQPitch = 41;             // uint4 per row of the q staging (5 groups x 8 + 1)
+constexpr int kOPitch = 260;            // floats per row of the output staging (16-byte stores at 4 wavefronts)
 
 // shared memory (bytes, from a 1 KB aligned base)
 constexpr int kOffA = 0;                                     // [kNB] plane sets
@@ -90,6 +92,8 @@ constexpr int kSmem = kOffMisc + 64;
 static_assert(kOffQR % 1024 == 0 && kPlane % 1024 == 0, "swizzled operands need 1 KB alignment");
 static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory budget (with 1 KB alignment slack)");
+static_assert(kRows * kOPitch * 4 <= kNB * kABuf, "output staging fits the plane buffers");
+static_assert(kRows * kQPitch * 16 <= kNB * kABuf, "q staging fits the plane buffers");
 
 // mbarriers
 constexpr int kBarAFull = 0;    // [kNB] count 128 (unpack threads)
@@ -300,6 +304,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // page ids of the split's packed pages (the planner caps a split at 64)
   for (int k = tid; k < min(n_pk, 64); k += kThreads)
     s_pages[k] = a.block_table[(long long)b * a.max_pages + sw.page_begin + k];
+  // this CTA's q rows (its four content groups and the RoPE group, 640 bytes a
+  // row) staged in the plane buffers with one round of coalesced loads;
+  // the softmax warps convert them below, before any plane is written.  Row
+  // pitch 656 bytes: a warp's 16-byte loads of 32 rows take four wavefronts.
+  // (all loads are issued before the first store: the compiler cannot move a
+  // global load past a shared store it might alias)
+  uint4* sQ = reinterpret_cast<uint4*>(sA);
+  {
+    constexpr int kQU = (kRows * 40 + kThreads - 1) / kThreads;
+    uint4 qv[kQU];
+#pragma unroll
+    for (int k = 0; k < kQU; ++k) {
+      const int u = tid + k * kThreads;
+      if (u < kRows * 40) {
+        const int h = u / 40, rem = u - 40 * h, j = rem >> 3;
+        const int g = j < 4 ? 4 * r + j : 8;
+        qv[k] = reinterpret_cast<const uint4*>(a.q + ((long long)b * a.H + hb + h) * kDim + 64 * g)[rem & 7];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kQU; ++k) {
+      const int u = tid + k * kThreads;
+      if (u < kRows * 40) sQ[(u / 40) * kQPitch + u % 40] = qv[k];
+    }
+  }
   // RoPE q block: row h, chunk c holds the channels in the unpack's order (each
   // rank multiplies only its half of them)
   {
@@ -335,13 +364,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   float qs[kMaxOwn] = {0.f, 0.f, 0.f, 0.f, 0.f};
   if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 8) {
     const int qd = warp & 3, th = (warp - kSoftWarp0) >> 2, h = 32 * qd + lane;
-    const uint16_t* qrow = a.q + ((long long)b * a.H + hb + h) * kDim;
 #pragma unroll
     for (int j = 0; j < kMaxOwn; ++j) {
-      const int g = j < 4 ? 4 * r + j : 8;
       const bool tb = j < 4 && kTypeB;
       uint32_t w[32];
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * g);
+      const uint4* src = sQ + h * kQPitch + 8 * j;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint4 v = src[k];
@@ -876,17 +903,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float* orow = a.part_o + ((long long)sidx * a.H + hb + h) * kLatent;
     if (done) {
       tc::tc_fence_after();
+      // my 128 columns of row h go to shared memory in channel order (the
+      // plane buffers are free: every MMA has completed and the unpack warps
+      // are done), then the CTA's 128 rows x 256 channels leave as coalesced
+      // 16-byte stores.  Positions 0, 2, 4, 6 of a chunk hold four adjacent
+      // channels and positions 1, 3, 5, 7 the next four.
+      float* sO = reinterpret_cast<float*>(sA);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        const int j = 2 * th + (c >> 1), g = 4 * r + j;
+        const int j = 2 * th + (c >> 1);
         const float mt = sX[(1 + j) * kRows + h] + sX[(6 + j) * kRows + h];
         float v[32];
         tmem_ld32(tl + kColO + 128 * th + 32 * c, v);
+        float* dst = sO + h * kOPitch + j * 64;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int cc = 32 * (c & 1) + e;
-          orow[g * 64 + tc::chan_of_pos(cc >> 3, cc & 7, kTypeB)] = v[e] + mt;
+        for (int k8 = 0; k8 < 4; ++k8) {
+          const int ck = 4 * (c & 1) + k8;  // chunk of the group
+          const float* u = v + 8 * k8;
+          *reinterpret_cast<float4*>(dst + tc::chan_of_pos(ck, 0, kTypeB)) =
+              make_float4(u[0] + mt, u[2] + mt, u[4] + mt, u[6] + mt);
+          *reinterpret_cast<float4*>(dst + tc::chan_of_pos(ck, 1, kTypeB)) =
+              make_float4(u[1] + mt, u[3] + mt, u[5] + mt, u[7] + mt);
         }
+      }
+      soft_sync();
+      const int st = tid - kSoftWarp0 * 32;  // 0..255
+      float* obase = a.part_o + ((long long)sidx * a.H + hb) * kLatent + 256 * r;
+#pragma unroll 4
+      for (int k = 0; k < kRows * 64 / kSoftThreads; ++k) {
+        const int idx = st + kSoftThreads * k;  // row idx / 64, float4 column idx % 64
+        const int row = idx >> 6, c4 = idx & 63;
+        *reinterpret_cast<float4*>(obase + (long long)row * kLatent + 4 * c4) =
+            *reinterpret_cast<const float4*>(sO + row * kOPitch + 4 * c4);
       }
       if (r == 0 && th == 0) {
         a.part_ml[((long long)sidx * a.H + hb + h) * 2] = m_run;
