@@ -17,7 +17,6 @@ constexpr int kMaxHeads = 128;
 constexpr int kMaxQueries = 16;                    // queries per sequence (multi-query decode)
 constexpr int kMaxRows = kMaxHeads * kMaxQueries;  // rows of a sequence in a plan
 constexpr int kCtasPerSm = 1;
-constexpr long long kMaxChunkPages = 64;
 
 int check_layout(const mla_lowbit_layout* l) {
   if (!l) return MLA_LOWBIT_ENULL;
@@ -140,31 +139,33 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   }
   const long long head_chunks =
       decode_ctas_per_split(layout->content_bits, heads, layout->rotate);
+  const long long max_chunk = decode_max_split_pages(layout->content_bits, heads, layout->rotate);
   const long long slots = (long long)num_sms * kCtasPerSm;
   // equal chunks of work units (pages, then the protected tokens' bf16 tiles)
   // so that all splits of all head chunks fit one wave when they can
   long long chunk = (work * head_chunks + slots - 1) / slots;
   if (chunk < 1) chunk = 1;
-  // a split accumulates at most kMaxChunkPages * 64 tokens in fp32 tensor-core
-  // accumulators (whose adds are not round-to-nearest); longer sequences get
-  // more splits, merged in fp32 by the combine kernel.  With several waves,
+  // a split accumulates at most max_chunk * 64 tokens in fp32 tensor-core
+  // accumulators (whose adds are not round-to-nearest; 64 or 128 pages by
+  // kernel); longer sequences get more splits, merged in fp32 by the combine
+  // kernel.  With several waves,
   // the work is spread evenly over all of them rather than leaving a sliver
   // for the last one; then the chunk grows until the per-sequence rounding
   // of the splits fits those waves.
   // If no chunk up to the cap fits that many waves, the next wave count is
   // tried, starting from the fewest waves that the capped chunk allows.
   long long total = 0;
-  for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)kMaxChunkPages);
-  long long waves = (chunk + kMaxChunkPages - 1) / kMaxChunkPages;
+  for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)max_chunk);
+  long long waves = (chunk + max_chunk - 1) / max_chunk;
   waves = std::max(waves, (total * head_chunks + slots - 1) / slots);
   for (;; ++waves) {
     chunk = (work * head_chunks + slots * waves - 1) / (slots * waves);
     if (chunk < 1) chunk = 1;
-    if (chunk > kMaxChunkPages) chunk = kMaxChunkPages;
+    if (chunk > max_chunk) chunk = max_chunk;
     for (;;) {
       total = 0;
       for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
-      if (total * head_chunks <= slots * waves || chunk >= kMaxChunkPages) break;
+      if (total * head_chunks <= slots * waves || chunk >= max_chunk) break;
       ++chunk;
     }
     if (total * head_chunks <= slots * waves || chunk == 1) break;

@@ -187,6 +187,10 @@ bool decode_fuses_append(int cbits, int rotate, int rows);
 // 128-row block for the tcgen05 kernel): the planner sizes chunks so that all
 // fit one wave.
 int decode_ctas_per_split(int cbits, int rows, int rotate);
+// Most work units (pages) one split may hold: it bounds the number of
+// accumulating MMAs into one fp32 tensor-core output (whose adds are not
+// round-to-nearest) and the split's page list in shared memory.
+int decode_max_split_pages(int cbits, int rows, int rotate);
 cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stream);
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (device, kernel): the limit is a per-device attribute.

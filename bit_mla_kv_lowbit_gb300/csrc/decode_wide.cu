@@ -84,8 +84,8 @@ constexpr int kOffShift = kOffMeta + kNB * kMaxOwn * 64 * 4; // [kNB][64] fp32 t
 constexpr int kOffValid = kOffShift + kNB * 64 * 4;          // [kNB][4] 16-token masks
 constexpr int kOffMax = kOffValid + kNB * 4 * 4;             // [2][2][128] fp32
 constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
-constexpr int kOffPages = kOffScan + 32 * 4;                 // [64] page ids of the split
-constexpr int kOffBar = kOffPages + 64 * 4;
+constexpr int kOffPages = kOffScan + 32 * 4;                 // [128] page ids of the split
+constexpr int kOffBar = kOffPages + 128 * 4;
 constexpr int kNumBars = 25;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
 constexpr int kSmem = kOffMisc + 64;
@@ -301,8 +301,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // page ids of the split's packed pages (the planner caps a split at 64)
-  for (int k = tid; k < min(n_pk, 64); k += kThreads)
+  // page ids of the split's packed pages (the planner caps a split at 128)
+  for (int k = tid; k < min(n_pk, 128); k += kThreads)
     s_pages[k] = a.block_table[(long long)b * a.max_pages + sw.page_begin + k];
   // this CTA's q rows (its four content groups and the RoPE group, 640 bytes a
   // row) staged in the plane buffers with one round of coalesced loads;

@@ -143,8 +143,10 @@ int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* 
  * every page), then, for packed layouts, its protected bf16 tokens (sink and
  * recent) in 64-token tiles of 3 units each.  The list is cut into splits of
  * `chunk_pages` units, chosen from the total work and the SM count so that all
- * splits of the call fit one wave when they can, and at most 64 so that no
- * split accumulates more than 4096 tokens; a bf16 tile belongs to the split
+ * splits of the call fit one wave when they can, and at most 128 (the
+ * 128-row cluster kernel: heads a multiple of 128 on a packed layout without
+ * rotation) or 64 (the 16-row kernel), which bounds the tokens one split
+ * accumulates in fp32 tensor-core outputs; a bf16 tile belongs to the split
  * that holds its first unit.  Writes the number of splits and the workspace
  * bytes the call needs.  num_sms == 0 asks the current CUDA device. */
 int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int heads,

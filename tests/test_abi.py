@@ -184,21 +184,28 @@ def test_plan_fills_one_wave_on_uniform_lengths():
 
 def test_plan_spreads_work_over_full_waves():
     # one CTA per SM; 128 heads run as 2-CTA clusters.  The planner picks the
-    # fewest waves the 64-page cap allows, then the smallest chunk whose splits
-    # fit those waves, so the last wave is not a short tail.
+    # fewest waves the split cap allows (128 pages for the cluster kernel, 64
+    # for the 16-row kernel), then the smallest chunk whose splits fit those
+    # waves, so the last wave is not a short tail.
     lay = pkg.layout(4, 4)
     for heads, lens in [(128, [8192] * 32), (128, [131072] * 4), (128, [10240] * 32),
                         (16, [2000] * 1000), (16, [32768] * 8)]:
         total, chunk, _ = pkg.decode_plan(lay, heads, lens, num_sms=152)
         cps = 2 * (heads // 128) if heads % 128 == 0 else heads // 16
-        assert 1 <= chunk <= 64
+        cap = 128 if heads % 128 == 0 else 64
+        assert 1 <= chunk <= cap
         waves = -(-total * cps // 152)
-        capped = sum(_expected_splits(L, True, 64) for L in lens)
+        capped = sum(_expected_splits(L, True, cap) for L in lens)
         assert waves == -(-capped * cps // 152) or waves == -(-total * cps // 152)
         assert waves >= -(-capped * cps // 152)          # never fewer than possible
         if chunk > 1:                                      # smallest chunk for these waves
             smaller = sum(_expected_splits(L, True, chunk - 1) for L in lens)
             assert smaller * cps > waves * 152
-    # the two cases that motivated it
-    assert pkg.decode_plan(lay, 128, [8192] * 32, num_sms=152)[:2] == (128, 34)
-    assert pkg.decode_plan(lay, 128, [131072] * 4, num_sms=152)[:2] == (152, 55)
+    # the cases that motivated it: one wave each (32 x 131 units in chunks of 68;
+    # 4 x 8,201 units in chunks of 109 -> 76 clusters), and several waves past
+    # the cap (4 x 1M tokens: chunks of 124, 532 splits)
+    assert pkg.decode_plan(lay, 128, [8192] * 32, num_sms=152)[:2] == (64, 68)
+    assert pkg.decode_plan(lay, 128, [131072] * 4, num_sms=152)[:2] == (76, 109)
+    assert pkg.decode_plan(lay, 128, [1048576] * 4, num_sms=152)[:2] == (532, 124)
+    # rotation runs on the 16-row kernel: the 64-page cap
+    assert pkg.decode_plan(pkg.layout(4, 4, rotate=True), 128, [131072] * 4, num_sms=152)[1] <= 64
