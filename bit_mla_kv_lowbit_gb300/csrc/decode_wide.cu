@@ -436,8 +436,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (n_ok) {
         // groups 4r + 2gh, 4r + 2gh + 1 are contiguous in the row
         const uint4* cs = reinterpret_cast<const uint4*>(crow + (CB == 4 ? 32 : 16) * (4 * r + 2 * gh));
+        // thread gh = 1 walks the chunks from the middle (bank spread, below):
+        // its words come in that order, so that the loop indexes them directly
+        if constexpr (CB == 4) {
 #pragma unroll
-        for (int k = 0; k < (CB == 4 ? 4 : 2); ++k) nc[k] = cs[k];
+          for (int k = 0; k < 4; ++k) nc[k] = cs[k ^ gh];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint4 v = cs[k];
+            nc[k] = gh ? make_uint4(v.z, v.w, v.x, v.y) : v;
+          }
+        }
         nr = *reinterpret_cast<const uint2*>(pb + G.rope_off + t * G.rope_row + 16 * r + 8 * gh);
       }
       if (n_okt) {
@@ -539,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int k2 = 0; k2 < 8; ++k2) {
               const int kk = k2 ^ (gh << 2);
               uint32_t p[4];
-              unpack_int4(gh ? w[k2 ^ 4] : w[k2], p);
+              unpack_int4(w[k2], p);
               *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, kk)) =
                   make_uint4(hmul2u(p[0], hiA), hmul2u(p[1], hiA), hmul2u(p[2], hiA), hmul2u(p[3], hiA));
               *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, kk)) =
@@ -552,7 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int k2 = 0; k2 < 4; ++k2) {
               const int kk = k2 ^ (gh << 1);
               uint32_t p[8];
-              unpack_int2(gh ? w[k2 ^ 2] : w[k2], p);
+              unpack_int2(w[k2], p);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 *reinterpret_cast<uint4*>(p1 + tc::sw_chunk(t, 2 * kk + hh)) =
@@ -809,13 +819,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int lim = sw.n_tok - n_masked - (bf_first + (i - n_pk) * 64 + kTW * th);
         vmask &= lim <= 0 ? 0u : lim >= kTW ? 0xFFFFFFFFu : (1u << lim) - 1u;
       }
+      // (the max of the raw logits, scaled once: the scale is positive and
+      // rounding is monotonic, so this is the max of the scaled logits)
       float mx = -INFINITY;
+      if (vmask == 0xFFFFFFFFu) {
 #pragma unroll
-      for (int t = 0; t < kTW; ++t) {
-        S[t] = ((vmask >> t) & 1u) ? S[t] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, S[t]);
+        for (int t = 0; t < kTW; ++t) mx = fmaxf(mx, S[t]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < kTW; ++t) {
+          S[t] = ((vmask >> t) & 1u) ? S[t] : -INFINITY;
+          mx = fmaxf(mx, S[t]);
+        }
       }
-      sMax[((i & 1) * 2 + th) * kRows + h] = mx;
+      sMax[((i & 1) * 2 + th) * kRows + h] = mx * a.scale_log2;
       if (pair_any(!ok, qd)) break;  // both warps of the rows leave at the same tile
       // my reads of the peer's partial are done: one arrival per warp, issued
       // after the tile max so that it does not queue ahead of local accesses
@@ -845,10 +862,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       m_run = m_new;
+      // p = 2^(scale * S - m) in one rounding; masked tokens (S = -inf) give 0,
+      // also while no token of the row has been valid yet (m = -inf)
+      const float mneg = m_run == -INFINITY ? 0.f : -m_run;
       float lsum = 0.f;
 #pragma unroll
       for (int t = 0; t < kTW; ++t) {
-        S[t] = S[t] == -INFINITY ? 0.f : fast_exp2(S[t] - m_run);
+        S[t] = fast_exp2(fmaf(S[t], a.scale_log2, mneg));
         lsum += S[t];
       }
       l += lsum;
