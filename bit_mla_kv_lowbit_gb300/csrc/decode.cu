@@ -648,10 +648,10 @@ struct CombineArgs {
 constexpr int kCombineWarps = 2;  // 128-channel quarters per block
 constexpr int kCombineThreads = kCombineWarps * 32;
 
-// One warp per (sequence, head, 128-channel quarter).  Lane s holds split s's
-// weight 2^(m_s - M) (splits beyond 32 recompute theirs); every lane then sums
-// its 4 channels over the splits with the weight broadcast by shuffle: no
-// shared memory and no block barrier.  Launched as a programmatic dependent
+// One warp per (sequence, head, 128-channel quarter).  Lane s holds the
+// weights 2^(m_s - M) of splits s and s + 32 (splits beyond 64 recompute
+// theirs); every lane then sums its 4 channels over the splits with the
+// weight broadcast by shuffle: no shared memory and no block barrier.  Launched as a programmatic dependent
 // of the split kernel, it waits for the split kernel's results before reading
 // them.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
@@ -665,21 +665,27 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   n = min(max(n, 0), a.total_splits - off);
   const float* ml = a.part_ml + ((long long)off * a.H + h) * 2;
   const long long mstride = (long long)a.H * 2;
-  float m_mine = -INFINITY, l_mine = 0.f;  // split `lane`
+  // lane s holds splits s and s + 32 (weights by shuffle); splits from 64 on
+  // recompute theirs
+  float m1 = -INFINITY, l1 = 0.f, m2 = -INFINITY, l2 = 0.f;
   float M = -INFINITY;
   for (int s = lane; s < n; s += 32) {
     const float2 v = *reinterpret_cast<const float2*>(ml + s * mstride);
     if (s < 32) {
-      m_mine = v.x;
-      l_mine = v.y;
+      m1 = v.x;
+      l1 = v.y;
+    } else if (s < 64) {
+      m2 = v.x;
+      l2 = v.y;
     }
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float w_mine = (l_mine > 0.f && M != -INFINITY) ? fast_exp2(m_mine - M) : 0.f;
-  float den = w_mine * l_mine;
-  for (int s = lane + 32; s < n; s += 32) {
+  const float w1 = (l1 > 0.f && M != -INFINITY) ? fast_exp2(m1 - M) : 0.f;
+  const float w2 = (l2 > 0.f && M != -INFINITY) ? fast_exp2(m2 - M) : 0.f;
+  float den = w1 * l1 + w2 * l2;
+  for (int s = lane + 64; s < n; s += 32) {
     const float2 v = *reinterpret_cast<const float2*>(ml + s * mstride);
     den += v.y > 0.f ? fast_exp2(v.x - M) * v.y : 0.f;
   }
@@ -689,17 +695,28 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   const float* o = a.part_o + ((long long)off * a.H + h) * kLatent + c;
   const long long ostride = (long long)a.H * kLatent;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int n32 = min(n, 32);
-#pragma unroll 4
-  for (int s = 0; s < n32; ++s) {
-    const float w = __shfl_sync(0xffffffffu, w_mine, s);
-    const float4 v = *reinterpret_cast<const float4*>(o + s * ostride);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  // the first 64 splits in batches of 16 loads issued together (the partials
+  // are L2-resident: latency, not bandwidth, sets the time)
+  constexpr int kBatch = 16;
+  const int n64 = min(n, 64);
+  for (int s0 = 0; s0 < n64; s0 += kBatch) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (s0 + k < n64) v[k] = *reinterpret_cast<const float4*>(o + (s0 + k) * ostride);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (s0 + k < n64) {
+        const int sk = s0 + k;
+        const float w = __shfl_sync(0xffffffffu, sk < 32 ? w1 : w2, sk & 31);
+        acc.x = fmaf(w, v[k].x, acc.x);
+        acc.y = fmaf(w, v[k].y, acc.y);
+        acc.z = fmaf(w, v[k].z, acc.z);
+        acc.w = fmaf(w, v[k].w, acc.w);
+      }
+    }
   }
-  for (int s = 32; s < n; ++s) {
+  for (int s = 64; s < n; ++s) {
     const float2 mv = *reinterpret_cast<const float2*>(ml + s * mstride);
     const float w = mv.y > 0.f ? fast_exp2(mv.x - M) : 0.f;
     const float4 v = *reinterpret_cast<const float4*>(o + s * ostride);
