@@ -145,11 +145,20 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, device) -> Optional[int]:
+    """The given stream, or the current stream of the device the call runs on."""
     torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return stream.cuda_stream
+
+
+def _same_device(device, **tensors):
+    """Every CUDA tensor of a call must be on the page pool's device: the
+    library launches on the current device, which the call sets to that one."""
+    for name, t in tensors.items():
+        if t is not None and t.device.type == "cuda" and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the page pool on {device}")
 
 
 def _expect(t, name, dtype, shape=None, device=True):
@@ -190,10 +199,14 @@ def write(lay: Layout, ckv, krope, pos, block_table, page_pool, sink_buf, recent
     pb = page_bytes(lay)
     if page_pool.dim() != 2 or page_pool.shape[1] != pb:
         raise ValueError(f"page_pool must be [num_pages][{pb}] uint8")
-    st = load().mla_lowbit_write(ctypes.byref(lay), n, _ptr(ckv), _ptr(krope), _ptr(seq_idx),
-                                 _ptr(pos), _ptr(seq_lens_after), num_seqs, _ptr(block_table),
-                                 max_pages, _ptr(page_pool), page_pool.shape[0], _ptr(sink_buf),
-                                 _ptr(recent_buf), _ptr(err_word), _stream(stream))
+    _same_device(page_pool.device, ckv=ckv, krope=krope, pos=pos, block_table=block_table,
+                 sink_buf=sink_buf, recent_buf=recent_buf, err_word=err_word, seq_idx=seq_idx,
+                 seq_lens_after=seq_lens_after)
+    with torch.cuda.device(page_pool.device):
+        st = load().mla_lowbit_write(ctypes.byref(lay), n, _ptr(ckv), _ptr(krope), _ptr(seq_idx),
+                                     _ptr(pos), _ptr(seq_lens_after), num_seqs, _ptr(block_table),
+                                     max_pages, _ptr(page_pool), page_pool.shape[0], _ptr(sink_buf),
+                                     _ptr(recent_buf), _ptr(err_word), _stream(stream, page_pool.device))
     _check(st, "mla_lowbit_write")
 
 
@@ -219,11 +232,14 @@ def decode(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host, sink
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     if lens.shape != (B,):
         raise ValueError("seq_lens_host must have one entry per sequence")
-    st = load().mla_lowbit_decode(
-        ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
-        page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-        lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
-        _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream))
+    _same_device(page_pool.device, q=q, block_table=block_table, seq_lens=seq_lens, sink_buf=sink_buf,
+                 recent_buf=recent_buf, out=out, workspace=workspace, err_word=err_word, lse=lse)
+    with torch.cuda.device(page_pool.device):
+        st = load().mla_lowbit_decode(
+            ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
+            page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+            lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream, page_pool.device))
     _check(st, "mla_lowbit_decode")
 
 
@@ -253,12 +269,16 @@ def write_decode(lay: Layout, q, ckv_new, krope_new, page_pool, block_table, seq
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     if lens.shape != (B,):
         raise ValueError("seq_lens_host must have one entry per sequence")
-    st = load().mla_lowbit_write_decode(
-        ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(ckv_new),
-        _ptr(krope_new), _ptr(page_pool), page_pool.shape[0], _ptr(block_table),
-        block_table.shape[1], _ptr(seq_lens), lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf),
-        _ptr(recent_buf), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-        _ptr(err_word), _stream(stream))
+    _same_device(page_pool.device, q=q, ckv_new=ckv_new, krope_new=krope_new, block_table=block_table,
+                 seq_lens=seq_lens, sink_buf=sink_buf, recent_buf=recent_buf, out=out,
+                 workspace=workspace, err_word=err_word, lse=lse)
+    with torch.cuda.device(page_pool.device):
+        st = load().mla_lowbit_write_decode(
+            ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(ckv_new),
+            _ptr(krope_new), _ptr(page_pool), page_pool.shape[0], _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf),
+            _ptr(recent_buf), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _ptr(err_word), _stream(stream, page_pool.device))
     _check(st, "mla_lowbit_write_decode")
 
 
@@ -285,11 +305,14 @@ def decode_multi(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_host
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     if lens.shape != (B,):
         raise ValueError("seq_lens_host must have one entry per sequence")
-    st = load().mla_lowbit_decode_multi(
-        ctypes.byref(lay), B, n, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
-        page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-        lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
-        _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream))
+    _same_device(page_pool.device, q=q, block_table=block_table, seq_lens=seq_lens, sink_buf=sink_buf,
+                 recent_buf=recent_buf, out=out, workspace=workspace, err_word=err_word, lse=lse)
+    with torch.cuda.device(page_pool.device):
+        st = load().mla_lowbit_decode_multi(
+            ctypes.byref(lay), B, n, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
+            page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+            lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(stream, page_pool.device))
     _check(st, "mla_lowbit_decode_multi")
 
 
@@ -319,11 +342,14 @@ def decode_noalloc(lay: Layout, q, page_pool, block_table, seq_lens, seq_lens_ho
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     if lens.shape != (B,):
         raise ValueError("seq_lens_host must have one entry per sequence")
-    st = load().mla_lowbit_decode_noalloc(
-        ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
-        page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-        lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
-        _ptr(lse), _ptr(err_word), _stream(stream))
+    _same_device(page_pool.device, q=q, block_table=block_table, seq_lens=seq_lens, sink_buf=sink_buf,
+                 recent_buf=recent_buf, out=out, err_word=err_word, lse=lse)
+    with torch.cuda.device(page_pool.device):
+        st = load().mla_lowbit_decode_noalloc(
+            ctypes.byref(lay), B, H, ctypes.c_float(softmax_scale), _ptr(q), _ptr(page_pool),
+            page_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+            lens.ctypes.data_as(ctypes.c_void_p), _ptr(sink_buf), _ptr(recent_buf), _ptr(out),
+            _ptr(lse), _ptr(err_word), _stream(stream, page_pool.device))
     _check(st, "mla_lowbit_decode_noalloc")
 
 
@@ -336,7 +362,9 @@ def set_fault_injection(mode: int, wait_cycles: int = 0) -> None:
 
 
 def read_error(err_word) -> int:
+    torch = _torch()
     code = ctypes.c_int32()
-    _check(load().mla_lowbit_read_error(_ptr(err_word), ctypes.byref(code)),
-           "mla_lowbit_read_error")
+    with torch.cuda.device(err_word.device):
+        _check(load().mla_lowbit_read_error(_ptr(err_word), ctypes.byref(code)),
+               "mla_lowbit_read_error")
     return code.value
