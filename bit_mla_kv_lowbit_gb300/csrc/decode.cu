@@ -774,11 +774,12 @@ static cudaError_t launch_combine(const CombineArgs& ca, cudaStream_t stream) {
 }
 
 // Kernel for a layout and a row count (n_q * heads), fixed by those alone:
-// packed caches with a multiple of 128 rows and no rotation take the 2-CTA
-// tcgen05 kernel (decode_wide.cu, one cluster per split and 128-row block);
-// everything else the mma.sync kernel above in 16-row chunks.
+// a multiple of 128 rows without rotation takes the 2-CTA tcgen05 kernel
+// (decode_wide.cu, one cluster per split and 128-row block; packed or bf16
+// pages); everything else the mma.sync kernel above in 16-row chunks.
 static bool use_wide(int cbits, int rotate, int rows) {
-  return cbits != 16 && !rotate && rows % 128 == 0;
+  (void)cbits;
+  return !rotate && rows % 128 == 0;
 }
 
 // 128 pages for the cluster kernel (8,192 tokens: max-abs 7.4e-4 against the

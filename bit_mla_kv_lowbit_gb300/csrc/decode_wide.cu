@@ -64,6 +64,7 @@ constexpr int kIssuerWarp = 12;      // QK
 constexpr int kPvWarp = 13;          // PV
 constexpr int kTW = 32;                 // tokens of a tile per softmax warp
 constexpr int kNB = 2;                  // plane-set ring depth (tiles)
+constexpr int kNBF = 4;                 // the same for bf16 pages (half the planes per tile)
 constexpr int kMaxOwn = 5;              // QK groups of a CTA
 constexpr int kPlane = 64 * 128;        // 64 tokens x 64 fp16 (128-byte rows)
 constexpr int kABuf = 2 * kMaxOwn * kPlane;  // s_hi planes of the 5 groups, then s_lo planes
@@ -81,12 +82,12 @@ constexpr int kOffQR = kOffA + kNB * kABuf;                  // RoPE q block
 constexpr int kOffX = kOffQR + kQBlock;
 constexpr int kOffMeta = kOffX + 2 * 8 * kRows * 16;         // [kNB][5][64] fp32 m'
 constexpr int kOffShift = kOffMeta + kNB * kMaxOwn * 64 * 4; // [kNB][64] fp32 token factor
-constexpr int kOffValid = kOffShift + kNB * 64 * 4;          // [kNB][4] 16-token masks
-constexpr int kOffMax = kOffValid + kNB * 4 * 4;             // [2][2][128] fp32
+constexpr int kOffValid = kOffShift + kNB * 64 * 4;          // [kNBF][4] 16-token masks
+constexpr int kOffMax = kOffValid + kNBF * 4 * 4;            // [2][2][128] fp32
 constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
 constexpr int kOffPages = kOffScan + 32 * 4;                 // [128] page ids of the split
 constexpr int kOffBar = kOffPages + 128 * 4;
-constexpr int kNumBars = 25;
+constexpr int kNumBars = 29;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
 constexpr int kSmem = kOffMisc + 64;
 static_assert(kOffQR % 1024 == 0 && kPlane % 1024 == 0, "swizzled operands need 1 KB alignment");
@@ -96,16 +97,16 @@ static_assert(kRows * kOPitch * 4 <= kNB * kABuf, "output staging fits the plane
 static_assert(kRows * kQPitch * 16 <= kNB * kABuf, "q staging fits the plane buffers");
 
 // mbarriers
-constexpr int kBarAFull = 0;    // [kNB] count 128 (unpack threads)
-constexpr int kBarAFree = 2;    // [kNB] count 1 (issuer commit after the tile's PV)
-constexpr int kBarDFull = 4;    // count 1: the tile's QK is complete
-constexpr int kBarDFree = 5;    // count 256: the softmax warps have read it
-constexpr int kBarPFull = 6;    // count 256: P of the tile is in tensor memory
-constexpr int kBarPFree = 7;    // count 1: the tile's PV is complete
-constexpr int kBarFlush = 8;    // count 2: final drain of both issuers
-constexpr int kBarXFull = 9;    // [8] per softmax warp w: count 1 + 4 KB of transactions, the peer's
+constexpr int kBarAFull = 0;    // [kNB or kNBF] count 128 (unpack or copy threads)
+constexpr int kBarAFree = 4;    // [kNB or kNBF] count 1 (issuer commit after the tile's PV)
+constexpr int kBarDFull = 8;    // count 1: the tile's QK is complete
+constexpr int kBarDFree = 9;    // count 256: the softmax warps have read it
+constexpr int kBarPFull = 10;   // count 256: P of the tile is in tensor memory
+constexpr int kBarPFree = 11;   // count 1: the tile's PV is complete
+constexpr int kBarFlush = 12;   // count 2: final drain of both issuers
+constexpr int kBarXFull = 13;   // [8] per softmax warp w: count 1 + 4 KB of transactions, the peer's
                                 //     warp w has written its partial logits into my buffer
-constexpr int kBarXFree = 17;   // [8] per softmax warp w: count 1, the peer's warp w has read its buffer
+constexpr int kBarXFree = 21;   // [8] per softmax warp w: count 1, the peer's warp w has read its buffer
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;     // [4 groups][64 channels] fp32
@@ -126,6 +127,12 @@ __device__ __forceinline__ void scale_by_token(float (&v)[kTW], const float4* f4
     v[4 * t4 + 2] *= f.z;
     v[4 * t4 + 3] *= f.w;
   }
+}
+
+// 16-byte global -> shared copy through L2 (cp.async; completion by group).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
 // OR of `pred` over the 256 softmax threads (named barrier 1).
@@ -234,6 +241,9 @@ __device__ __forceinline__ int chan_at(int p, bool tb) { return tc::chan_of_pos(
 template <int CB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_wide_kernel(DecodeArgs a) {
+  constexpr bool kBF = CB == 16;     // bf16 pages: planes are the values themselves
+  constexpr int NB = kBF ? kNBF : kNB;           // plane-set ring depth
+  constexpr int ABUF = kBF ? kABuf / 2 : kABuf;  // bytes per plane set (bf16: no s_lo planes)
   constexpr bool kTypeB = CB == 2;
   constexpr PageGeom G = page_geom(CB);
   constexpr float kCentreC = kTypeB ? float(kCentre2) : float(kCentre4);
@@ -261,7 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int hb = kRows * blockIdx.y;  // first query row of this cluster
 
   int b, split, nsplit;
-  find_split<kThreads>(a, true, scan, b, split, nsplit, sidx);
+  find_split<kThreads>(a, !kBF, scan, b, split, nsplit, sidx);
   if (b < 0) return;  // both CTAs of the cluster name the same split
   const int L = [&] {
     const int v = a.seq_lens[b];
@@ -271,7 +281,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     a.seq_split[2 * b] = sidx;
     a.seq_split[2 * b + 1] = nsplit;
   }
-  const SplitWork sw = split_work(L, split, a.chunk_pages, true);
+  const SplitWork sw = split_work(L, split, a.chunk_pages, !kBF);
   const int n_pk = sw.n_pages;
   const int bf_first = 64 * sw.bf_begin;
   const int bf_end = min(sw.n_tok, 64 * (sw.bf_begin + sw.n_bf));
@@ -279,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, TMEM, page ids, RoPE q block
   if (tid == 0) {
-    for (int i = 0; i < kNB; ++i) {
+    for (int i = 0; i < kNBF; ++i) {
       tc::bar_init(bar(kBarAFull + i), kUnpackThreads);
       tc::bar_init(bar(kBarAFree + i), 1);
     }
@@ -331,7 +341,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   // RoPE q block: row h, chunk c holds the channels in the unpack's order (each
   // rank multiplies only its half of them)
-  {
+  if constexpr (kBF) {
+    // bf16 pages: the row's RoPE channels in their own order, unconverted
+    for (int u = tid; u < kRows * 8; u += kThreads) {
+      const int h = u >> 3, c = u & 7;
+      *reinterpret_cast<uint4*>(sQR + tc::sw_chunk(h, c)) =
+          reinterpret_cast<const uint4*>(a.q + ((long long)b * a.H + hb + h) * kDim + 512)[c];
+    }
+  } else {
     for (int u = tid; u < kRows * 4; u += kThreads) {
       const int h = u >> 2, cc = u & 3;
       const uint4* src = reinterpret_cast<const uint4*>(a.q + ((long long)b * a.H + hb + h) * kDim + 512 + 16 * cc);
@@ -378,6 +395,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float acc = 0.f;
 #pragma unroll
       for (int p2 = 0; p2 < 32; ++p2) {
+        if constexpr (kBF) {  // bf16 pages: q stays bf16, channels in order
+          o[p2] = w[p2];
+          continue;
+        }
         const int c0 = tb ? chan_at(2 * p2, true) : chan_at(2 * p2, false);
         const int c1 = tb ? chan_at(2 * p2 + 1, true) : chan_at(2 * p2 + 1, false);
         const float f0 = (c0 & 1) ? bf16hi_to_f32(w[c0 >> 1]) : bf16lo_to_f32(w[c0 >> 1]);
@@ -396,7 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
     }
-    if (th == 0) {
+    if (th == 0 && !kBF) {
       float qh[kMaxOwn], qm[kMaxOwn], ql[kMaxOwn];
 #pragma unroll
       for (int j = 0; j < kMaxOwn; ++j) split3_bf16(qs[j], qh[j], qm[j], ql[j]);
@@ -411,7 +432,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote arrive or store
 
-  if (warp < 4) {
+  if (warp < 4 && kBF) {
+    // ---------------- copy (bf16 pages): token t of every tile; thread half gh
+    // moves content groups 4r + 2gh, 4r + 2gh + 1 and RoPE channels
+    // 32r + 16gh .. +15 of the page row into the planes with 16-byte cp.async,
+    // kNBF - 1 tiles ahead; an invalid row (past the sequence, or a bad page)
+    // is written as zeros.  A tile is handed over once its copies are complete
+    // (wait_group) and visible to the tensor core (proxy fence).
+    const int t = tid >> 1, gh = tid & 1;
+    auto issue = [&](int i) {
+      uint8_t* A = sA + (i % NB) * ABUF;
+      const long long page = s_pages[i];
+      const bool ok_p = page >= 0 && page < a.num_pages;
+      if (!ok_p && tid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+      const bool okt = ok_p && (sw.page_begin + i) * kPageTokens + t < L;
+      const uint8_t* row = a.pool + (ok_p ? page : 0) * (long long)G.page_bytes + t * G.content_row;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * gh + jj;
+        uint8_t* p1 = A + j * kPlane;
+#pragma unroll
+        for (int c2 = 0; c2 < 8; ++c2) {
+          const int c = c2 ^ (gh << 2);  // the token's two threads walk the chunks in different orders
+          uint8_t* dst = p1 + tc::sw_chunk(t, c);
+          if (okt) {
+            cp_async16(dst, row + 128 * (4 * r + j) + 16 * c);
+          } else {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int c = 4 * r + 2 * gh + k2;
+        uint8_t* dst = A + 4 * kPlane + tc::sw_chunk(t, c);
+        if (okt) {
+          cp_async16(dst, row + 1024 + 16 * c);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    for (int i = 0; i < NB - 1; ++i) {
+      if (i < n_pk) {
+        issue(i);
+      } else {
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+    }
+    for (int i = 0; i < n_tiles; ++i) {
+      const int buf = i % NB;
+      // this tile's copies are complete (the NB - 2 later groups may still run)
+      asm volatile("cp.async.wait_group %0;" ::"n"(kNBF - 2) : "memory");
+      tc::fence_async_smem();
+      const bool okt = i < n_pk && s_pages[i] >= 0 && s_pages[i] < a.num_pages &&
+                       (sw.page_begin + i) * kPageTokens + t < L;
+      uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
+      mk = (mk | (mk >> 1)) & 0x33333333u;
+      mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
+      mk = (mk | (mk >> 4)) & 0x00FF00FFu;
+      mk = (mk | (mk >> 8)) & 0x0000FFFFu;
+      if (lane == 0) sMask[buf * 4 + warp] = mk;
+      // self-test of the bounded waits: the first tile's hand-off is withheld
+      if (!(a.fault == 1 && i == 0)) tc::bar_arrive(bar(kBarAFull + buf));
+      // refill: tile i + NB - 1 goes to the buffer of tile i - 1, free once
+      // that tile's PV is complete
+      const int nxt = i + NB - 1;
+      if (nxt < n_pk) {
+        const bool free_ok =
+            i < 1 || wait(bar(kBarAFree + (i - 1) % NB), ((i - 1) / NB) & 1, abort_flag, a.err, a.wait_cycles);
+        if (!__all_sync(0xffffffffu, free_ok)) break;
+        issue(nxt);
+      } else {
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  } else if (warp < 4) {
     // ---------------- unpack: token t of every tile; thread half gh takes
     // content groups 2gh, 2gh+1 and RoPE words 4r+2gh, 4r+2gh+1 (16 channels)
     const int t = tid >> 1, gh = tid & 1;
@@ -666,8 +764,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // min-term k-steps
       const uint32_t id_min = id_qk | (1u << 7) | (1u << 10);
       const uint32_t id_pv = tc::idesc(128, 256, 0, 1);   // A (tensor memory), B MN-major
+      const uint32_t id_pv_bf = id_pv | (1u << 7) | (1u << 10);
       auto tile_ready = [&](int i) {
-        const bool r2 = wait(bar(kBarAFull + i % kNB), (i / kNB) & 1, abort_flag, a.err, a.wait_cycles);
+        const bool r2 = wait(bar(kBarAFull + i % NB), (i / NB) & 1, abort_flag, a.err, a.wait_cycles);
         if (r2) tc::tc_fence_after();
         return r2;
       };
@@ -683,31 +782,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!(tile_ready(k) && (k == 0 || wait(bar(kBarDFree), (k - 1) & 1, abort_flag, a.err, a.wait_cycles))))
             break;
           tc::tc_fence_after();
-          const uint64_t d = kq0 + (uint64_t)(((k % kNB) * kABuf) >> 4);
+          const uint64_t d = kq0 + (uint64_t)(((k % NB) * ABUF) >> 4);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint32_t qa = tmem + kColQ + 32 * j + 8 * ks;
-              mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, (j | ks) != 0);
-              mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
+              if constexpr (kBF) {  // bf16 q and values: one product, exact in fp32
+                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_min, (j | ks) != 0);
+              } else {
+                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, (j | ks) != 0);
+                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
+              }
             }
           }
           // this rank's half of the RoPE channels: k-steps 2r, 2r + 1
 #pragma unroll
           for (int k2 = 0; k2 < 2; ++k2) {
             const int ks = 2 * r + k2;
-            tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                    d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_qk, 1);
-            tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                    d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
+            if constexpr (kBF) {
+              tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                      d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+            } else {
+              tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                      d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_qk, 1);
+              tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                      d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
+            }
           }
           // the min terms: the other rank's RoPE k-steps, in bf16
+          if constexpr (!kBF) {
 #pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2) {
-            const int ks = 2 * (1 - r) + k2;
-            tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                    d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int ks = 2 * (1 - r) + k2;
+              tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
+                      d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+            }
           }
           tc::commit(bar(kBarDFull));
         }
@@ -717,19 +827,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // its QK (tested again here: an acquire in this thread too)
           if (!(wait(bar(kBarPFull), k & 1, abort_flag, a.err, a.wait_cycles) && tile_ready(k))) break;
           tc::tc_fence_after();
-          const uint64_t d = kp0 + (uint64_t)(((k % kNB) * kABuf) >> 4);
+          const uint64_t d = kp0 + (uint64_t)(((k % NB) * ABUF) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             // the four content groups' planes side by side: N = 256 channels
             const uint64_t b1 = d + (uint64_t)((2048 * ks) >> 4);
             const uint64_t b2 = d + (uint64_t)((kMaxOwn * kPlane + 2048 * ks) >> 4);
             const uint32_t phi = tmem + kColP + 8 * ks, plo = tmem + kColP + 32 + 8 * ks;
-            mma_tmem_a(tmem + kColO, phi, b1, id_pv, (k > 0 || ks > 0));
-            mma_tmem_a(tmem + kColO, plo, b1, id_pv, 1);
-            mma_tmem_a(tmem + kColO, phi, b2, id_pv, 1);
+            if constexpr (kBF) {  // P in bf16 high and low parts, bf16 values
+              mma_tmem_a(tmem + kColO, phi, b1, id_pv_bf, (k > 0 || ks > 0));
+              mma_tmem_a(tmem + kColO, plo, b1, id_pv_bf, 1);
+            } else {
+              mma_tmem_a(tmem + kColO, phi, b1, id_pv, (k > 0 || ks > 0));
+              mma_tmem_a(tmem + kColO, plo, b1, id_pv, 1);
+              mma_tmem_a(tmem + kColO, phi, b2, id_pv, 1);
+            }
           }
           tc::commit(bar(kBarPFree));
-          tc::commit(bar(kBarAFree + k % kNB));
+          tc::commit(bar(kBarAFree + k % NB));
         }
       }
       // drain (bounded, regardless of the abort flag) before TMEM is freed:
@@ -768,7 +883,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     int done_tiles = 0;
     for (int i = 0; i < n_tiles; ++i) {
-      const int buf = i % kNB;
+      const int buf = i % NB;
       const bool packed_tile = i < n_pk;
       const float* meta = sMeta + buf * kMaxOwn * 64 + kTW * th;
       const float4* f4 = reinterpret_cast<const float4*>(sShift + buf * 64 + kTW * th);
@@ -777,7 +892,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // plus the min terms.  The unpack warps' metadata of this tile is read
       // after an acquire on its plane-ready barrier (complete by now: QK ran).
       if (ok) ok = wait(bar(kBarDFull), i & 1, abort_flag, a.err, a.wait_cycles);
-      if (ok) ok = wait(bar(kBarAFull + buf), (i / kNB) & 1, abort_flag, a.err, a.wait_cycles);
+      if (ok) ok = wait(bar(kBarAFull + buf), (i / NB) & 1, abort_flag, a.err, a.wait_cycles);
       const uint32_t mk0 = sMask[buf * 4 + 2 * th], mk1 = sMask[buf * 4 + 2 * th + 1];
       const bool shifted = ((mk0 | mk1) >> 31) != 0;  // some token's logit and P take a factor 16
       uint32_t vmask = (mk0 & 0xFFFFu) | ((mk1 & 0xFFFFu) << 16);
@@ -817,6 +932,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // row's query block also masks the last protected tokens.
       if (!packed_tile) {
         const int lim = sw.n_tok - n_masked - (bf_first + (i - n_pk) * 64 + kTW * th);
+        vmask &= lim <= 0 ? 0u : lim >= kTW ? 0xFFFFFFFFu : (1u << lim) - 1u;
+      } else if (kBF && n_masked > 0) {
+        // bf16 pages hold the last tokens too: the row's query block does not
+        // see the sequence's last n_masked of them
+        const int lim = L - n_masked - ((sw.page_begin + i) * kPageTokens + kTW * th);
         vmask &= lim <= 0 ? 0u : lim >= kTW ? 0xFFFFFFFFu : (1u << lim) - 1u;
       }
       // (the max of the raw logits, scaled once: the scale is positive and
@@ -877,7 +997,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // caches): the four sums rotate one place per group, back in order
       // after the fourth.
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < (kBF ? 0 : 4); ++j) {
         const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64);
         float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -900,7 +1020,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t hi[kTW / 2], lo[kTW / 2];
         if (shifted) scale_by_token(S, f4);
 #pragma unroll
-        for (int t2 = 0; t2 < kTW / 2; ++t2) split_trunc(S[2 * t2], S[2 * t2 + 1], hi[t2], lo[t2]);
+        for (int t2 = 0; t2 < kTW / 2; ++t2) {
+          if constexpr (kBF) {
+            split_trunc_bf16(S[2 * t2], S[2 * t2 + 1], hi[t2], lo[t2]);
+          } else {
+            split_trunc(S[2 * t2], S[2 * t2 + 1], hi[t2], lo[t2]);
+          }
+        }
         tmem_st16_nowait(tl + kColP + (kTW / 2) * th, hi);
         tmem_st16_nowait(tl + kColP + 32 + (kTW / 2) * th, lo);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -940,10 +1066,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k8 = 0; k8 < 4; ++k8) {
           const int ck = 4 * (c & 1) + k8;  // chunk of the group
           const float* u = v + 8 * k8;
-          *reinterpret_cast<float4*>(dst + tc::chan_of_pos(ck, 0, kTypeB)) =
-              make_float4(u[0] + mt, u[2] + mt, u[4] + mt, u[6] + mt);
-          *reinterpret_cast<float4*>(dst + tc::chan_of_pos(ck, 1, kTypeB)) =
-              make_float4(u[1] + mt, u[3] + mt, u[5] + mt, u[7] + mt);
+          if constexpr (kBF) {  // bf16 pages: channels in order
+            *reinterpret_cast<float4*>(dst + 8 * ck) = make_float4(u[0], u[1], u[2], u[3]);
+            *reinterpret_cast<float4*>(dst + 8 * ck + 4) = make_float4(u[4], u[5], u[6], u[7]);
+          } else {
+            *reinterpret_cast<float4*>(dst + tc::chan_of_pos(ck, 0, kTypeB)) =
+                make_float4(u[0] + mt, u[2] + mt, u[4] + mt, u[6] + mt);
+            *reinterpret_cast<float4*>(dst + tc::chan_of_pos(ck, 1, kTypeB)) =
+                make_float4(u[1] + mt, u[3] + mt, u[5] + mt, u[7] + mt);
+          }
         }
       }
       soft_sync();
@@ -984,7 +1115,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stream) {
   const int smem = wide::kSmem + 1024;
-  void (*kern)(DecodeArgs) = cbits == 4 ? wide::decode_wide_kernel<4> : wide::decode_wide_kernel<2>;
+  void (*kern)(DecodeArgs) = cbits == 4   ? wide::decode_wide_kernel<4>
+                             : cbits == 2 ? wide::decode_wide_kernel<2>
+                                          : wide::decode_wide_kernel<16>;
   const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.total_splits, a.H / wide::kRows), block(wide::kThreads);

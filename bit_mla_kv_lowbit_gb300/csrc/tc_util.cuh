@@ -299,5 +299,15 @@ __device__ __forceinline__ void split_trunc(float a, float b, uint32_t& hi, uint
   lo = pack_half2(a - ha, b - hb);
 }
 
+// The same in bf16: hi = x cut to 8 significant bits (its upper 16 bits, exact
+// in bf16), lo = the exact remainder rounded to bf16: x to about 2^-17
+// relative, with fp32's exponent range.  Pairs are (a, b) in (low, high) halves.
+__device__ __forceinline__ void split_trunc_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint32_t ua = __float_as_uint(a) & 0xFFFF0000u, ub = __float_as_uint(b) & 0xFFFF0000u;
+  hi = ub | (ua >> 16);
+  const float ra = a - __uint_as_float(ua), rb = b - __uint_as_float(ub);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(rb), "f"(ra));
+}
+
 }  // namespace tc
 }  // namespace mlalb

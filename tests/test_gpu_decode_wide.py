@@ -1,7 +1,7 @@
 """The 128-row tcgen05 decode (2-CTA clusters, decode_wide.cu) vs the fp64 oracle.
 
-Packed layouts with exactly 128 query rows per sequence (128 heads, or n_q
-query blocks of 128 / n_q heads) take this kernel by default.  Same bar as
+Packed layouts and bf16 pages with exactly 128 query rows per sequence (128
+heads, or n_q query blocks of 128 / n_q heads) take this kernel by default.  Same bar as
 the other decode tests: max-abs <= 2e-3 and rel-L2 <= 1e-3 per sequence, lse
 within 1e-4, writer bytes bit-exact.
 """
@@ -17,17 +17,20 @@ from workloads import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cb", [4, 2])
+@pytest.mark.parametrize("cb", [4, 2, 16])
 def test_wide_edge_lengths(cb):
-    w = syn.custom(f"wide_edge_c{cb}", EDGE_LENGTHS, heads=128, content_bits=cb, seed=81)
+    w = syn.custom(f"wide_edge_c{cb}", EDGE_LENGTHS, heads=128, content_bits=cb,
+                   rope_bits=16 if cb == 16 else 4, seed=81)
     run = GpuRun(w)
     run.prefill()
     _check_run_step(run, 0, lse=True)
 
 
-def test_wide_long_sequences_many_splits():
+@pytest.mark.parametrize("cb", [4, 16])
+def test_wide_long_sequences_many_splits(cb):
     # sequences long enough for several splits each, with a short one beside
-    w = syn.custom("wide_long", [17000, 9000, 133, 1], heads=128, content_bits=4, seed=82)
+    w = syn.custom(f"wide_long_c{cb}", [17000, 9000, 133, 1], heads=128, content_bits=cb,
+                   rope_bits=16 if cb == 16 else 4, seed=82)
     run = GpuRun(w)
     run.prefill()
     _check_run_step(run, 0, lse=True)
@@ -42,12 +45,12 @@ def test_wide_write_decode_steps():
         _check_run_step(run, s, lse=True, fused=True)
 
 
-@pytest.mark.parametrize("cb,heads,n", [(4, 64, 2), (4, 16, 8), (2, 32, 4)])
+@pytest.mark.parametrize("cb,heads,n", [(4, 64, 2), (4, 16, 8), (2, 32, 4), (16, 64, 2), (16, 32, 4)])
 def test_wide_multi_query_blocks(cb, heads, n):
     # n_q * heads = 128 rows: per-row causal masks inside the 128-row kernel
     import torch
     w = syn.custom(f"wide_mq_c{cb}_h{heads}_n{n}", [8, 131, 134, 700, 2500], heads=heads,
-                   content_bits=cb, steps=n, seed=85 + n)
+                   content_bits=cb, rope_bits=16 if cb == 16 else 4, steps=n, seed=85 + n)
     run = GpuRun(w)
     run.prefill()
     ckv, kr, _ = run.step_inputs(0)

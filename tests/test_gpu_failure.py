@@ -20,10 +20,12 @@ pytestmark = pytest.mark.gpu
 PIPELINE = 32
 
 
-def test_bounded_wait_runs_out_and_context_recovers():
+@pytest.mark.parametrize("cb", [4, 16])
+def test_bounded_wait_runs_out_and_context_recovers(cb):
     import torch
     import bit_mla_kv_lowbit_gb300 as pkg
-    w = syn.custom("fault128", [700, 2100, 140], heads=128, content_bits=4, steps=2, seed=91)
+    w = syn.custom(f"fault128_c{cb}", [700, 2100, 140], heads=128, content_bits=cb,
+                   rope_bits=16 if cb == 16 else 4, steps=2, seed=91)
     run = GpuRun(w)
     run.prefill()
     run.run_step(0)
@@ -56,9 +58,11 @@ def test_fault_setting_is_validated():
     pkg.set_fault_injection(0, 0)
 
 
-def test_bad_page_128_rows():
+@pytest.mark.parametrize("cb", [4, 16])
+def test_bad_page_128_rows(cb):
     import torch
-    w = syn.custom("badpage128", [700], heads=128, content_bits=4, seed=92)
+    w = syn.custom(f"badpage128_c{cb}", [700], heads=128, content_bits=cb,
+                   rope_bits=16 if cb == 16 else 4, seed=92)
     run = GpuRun(w)
     run.prefill()
     run.run_step(0)
@@ -75,9 +79,11 @@ def test_bad_page_128_rows():
     assert torch.isfinite(out).all()
 
 
-def test_host_device_length_mismatch_128_rows():
+@pytest.mark.parametrize("cb", [4, 16])
+def test_host_device_length_mismatch_128_rows(cb):
     import torch
-    w = syn.custom("mismatch128", [700, 300], heads=128, content_bits=4, seed=93)
+    w = syn.custom(f"mismatch128_c{cb}", [700, 300], heads=128, content_bits=cb,
+                   rope_bits=16 if cb == 16 else 4, seed=93)
     run = GpuRun(w)
     run.prefill()
     run.run_step(0)
