@@ -148,27 +148,47 @@ int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int he
   // a split accumulates at most max_chunk * 64 tokens in fp32 tensor-core
   // accumulators (whose adds are not round-to-nearest; 64 or 128 pages by
   // kernel); longer sequences get more splits, merged in fp32 by the combine
-  // kernel.  With several waves,
-  // the work is spread evenly over all of them rather than leaving a sliver
-  // for the last one; then the chunk grows until the per-sequence rounding
-  // of the splits fits those waves.
-  // If no chunk up to the cap fits that many waves, the next wave count is
-  // tried, starting from the fewest waves that the capped chunk allows.
-  long long total = 0;
-  for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)max_chunk);
+  // kernel.  For a wave count, the work is spread evenly over all its waves
+  // (no sliver for the last one): the smallest chunk, from the even share
+  // up, whose splits fit.
+  auto splits_for = [&](long long c) {
+    long long t = 0;
+    for (int b = 0; b < num_seqs; ++b) t += splits_of(seq_lens_host[b], packed, (int)c);
+    return t;
+  };
+  auto fit = [&](long long w, long long& c_out, long long& t_out) {
+    long long c = (work * head_chunks + slots * w - 1) / (slots * w);
+    c = std::min(std::max(c, 1LL), max_chunk);
+    for (;;) {
+      const long long t = splits_for(c);
+      if (t * head_chunks <= slots * w || c >= max_chunk) {
+        c_out = c;
+        t_out = t;
+        return t * head_chunks <= slots * w;
+      }
+      ++c;
+    }
+  };
+  // the fewest waves that the capped chunk allows, then more until one fits
+  // (or the chunk is down to one page)
+  long long total = splits_for(max_chunk);
   long long waves = (chunk + max_chunk - 1) / max_chunk;
   waves = std::max(waves, (total * head_chunks + slots - 1) / slots);
-  for (;; ++waves) {
-    chunk = (work * head_chunks + slots * waves - 1) / (slots * waves);
-    if (chunk < 1) chunk = 1;
-    if (chunk > max_chunk) chunk = max_chunk;
-    for (;;) {
-      total = 0;
-      for (int b = 0; b < num_seqs; ++b) total += splits_of(seq_lens_host[b], packed, (int)chunk);
-      if (total * head_chunks <= slots * waves || chunk >= max_chunk) break;
-      ++chunk;
+  for (;; ++waves)
+    if (fit(waves, chunk, total) || chunk == 1) break;
+  // A CTA's time is about its split's units plus a fixed set-up and epilogue
+  // (about kWaveUnits units), so the step takes waves * (chunk + kWaveUnits):
+  // one or two more waves of smaller chunks are taken when that is at least
+  // 5 % less (the per-sequence rounding can force a large chunk into the
+  // fewest waves; more splits also cost the combine a little).
+  constexpr long long kWaveUnits = 3;
+  for (long long w = waves + 1; w <= waves + 2; ++w) {
+    long long c2 = 0, t2 = 0;
+    if (fit(w, c2, t2) && 20 * w * (c2 + kWaveUnits) < 19 * waves * (chunk + kWaveUnits)) {
+      waves = w;
+      chunk = c2;
+      total = t2;
     }
-    if (total * head_chunks <= slots * waves || chunk == 1) break;
   }
   if (total > INT32_MAX / 2) return MLA_LOWBIT_ESIZE;
   *total_splits = (int)total;
