@@ -142,11 +142,13 @@ int mla_lowbit_write(const mla_lowbit_layout* layout, int n_tokens, const void* 
  * units: one per 64-token page that holds a packed-served token (bf16 pages:
  * every page), then, for packed layouts, its protected bf16 tokens (sink and
  * recent) in 64-token tiles of 3 units each.  The list is cut into splits of
- * `chunk_pages` units, chosen from the total work and the SM count so that all
- * splits of the call fit one wave when they can, and at most 128 (the
- * 128-row cluster kernel: heads a multiple of 128 on a packed layout without
- * rotation) or 64 (the 16-row kernel), which bounds the tokens one split
- * accumulates in fp32 tensor-core outputs; a bf16 tile belongs to the split
+ * `chunk_pages` units, chosen from the total work and the SM count: the
+ * fewest waves of CTAs (one per SM) that the cap allows, or one or two more
+ * waves of smaller chunks when the estimated time, waves x (chunk + 3), drops
+ * by at least 5 %; the smallest chunk whose splits fit the waves.  The cap is
+ * 128 units for the 128-row cluster kernel (query rows a multiple of 128,
+ * no rotation) and 64 for the 16-row kernel; it bounds the tokens one split
+ * accumulates in fp32 tensor-core outputs.  A bf16 tile belongs to the split
  * that holds its first unit.  Writes the number of splits and the workspace
  * bytes the call needs.  num_sms == 0 asks the current CUDA device. */
 int mla_lowbit_decode_plan(const mla_lowbit_layout* layout, int num_seqs, int heads,
