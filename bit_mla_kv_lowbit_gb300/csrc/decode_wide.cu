@@ -47,6 +47,11 @@
 // Every wait is bounded; on a time-out the CTA records MLA_LOWBIT_DEV_PIPELINE,
 // the softmax warps of a quadrant leave the tile loop together, the partial is
 // written empty, and tensor memory is still freed.
+#include <cuda.h>  // CUtensorMap and its encoding enums (the encoder comes through the runtime)
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "decode_common.cuh"
 #include "tc_util.cuh"
 
@@ -87,7 +92,7 @@ constexpr int kOffMax = kOffValid + kNBF * 4 * 4;            // [2][2][128] fp32
 constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
 constexpr int kOffPages = kOffScan + 32 * 4;                 // [128] page ids of the split
 constexpr int kOffBar = kOffPages + 128 * 4;
-constexpr int kNumBars = 29;
+constexpr int kNumBars = 33;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
 constexpr int kSmem = kOffMisc + 64;
 static_assert(kOffQR % 1024 == 0 && kPlane % 1024 == 0, "swizzled operands need 1 KB alignment");
@@ -107,6 +112,7 @@ constexpr int kBarFlush = 12;   // count 2: final drain of both issuers
 constexpr int kBarXFull = 13;   // [8] per softmax warp w: count 1 + 4 KB of transactions, the peer's
                                 //     warp w has written its partial logits into my buffer
 constexpr int kBarXFree = 21;   // [8] per softmax warp w: count 1, the peer's warp w has read its buffer
+constexpr int kBarTFull = 29;   // [kNBF] bf16 pages: count 1 + 40 KB of tensor-copy transactions
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;     // [4 groups][64 channels] fp32
@@ -129,10 +135,20 @@ __device__ __forceinline__ void scale_by_token(float (&v)[kTW], const float4* f4
   }
 }
 
-// 16-byte global -> shared copy through L2 (cp.async; completion by group).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+// One 2-D box of a tensor map into shared memory (the tensor-memory
+// accelerator), completing `bytes` of transactions on the barrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Bounded wait on a barrier phase that ignores the abort flag (copies in
+// flight must land before the CTA leaves).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!tc::bar_test(bar, parity))
+    if (clock64() - t0 > limit) break;
 }
 
 // OR of `pred` over the 256 softmax threads (named barrier 1).
@@ -240,7 +256,7 @@ __device__ __forceinline__ int chan_at(int p, bool tb) { return tc::chan_of_pos(
 
 template <int CB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_wide_kernel(DecodeArgs a) {
+    decode_wide_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   constexpr bool kBF = CB == 16;     // bf16 pages: planes are the values themselves
   constexpr int NB = kBF ? kNBF : kNB;           // plane-set ring depth
   constexpr int ABUF = kBF ? kABuf / 2 : kABuf;  // bytes per plane set (bf16: no s_lo planes)
@@ -292,6 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNBF; ++i) {
       tc::bar_init(bar(kBarAFull + i), kUnpackThreads);
       tc::bar_init(bar(kBarAFree + i), 1);
+      tc::bar_init(bar(kBarTFull + i), 1);
     }
     tc::bar_init(bar(kBarDFull), 1);
     tc::bar_init(bar(kBarDFree), kSoftThreads);
@@ -427,67 +444,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::fence_async_smem();
     }
   }
+  // the q staging's reads (generic proxy) come before any tensor copy
+  // (async proxy) into the same plane buffers
+  tc::fence_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote arrive or store
 
   if (warp < 4 && kBF) {
-    // ---------------- copy (bf16 pages): token t of every tile; thread half gh
-    // moves content groups 4r + 2gh, 4r + 2gh + 1 and RoPE channels
-    // 32r + 16gh .. +15 of the page row into the planes with 16-byte cp.async,
-    // kNBF - 1 tiles ahead; an invalid row (past the sequence, or a bad page)
-    // is written as zeros.  A tile is handed over once its copies are complete
-    // (wait_group) and visible to the tensor core (proxy fence).
+    // ---------------- copy (bf16 pages): thread 0 loads each tile's five
+    // planes (the CTA's four content groups and the RoPE group, 64 tokens x 64
+    // channels each) with the tensor-memory accelerator, kNBF - 1 tiles ahead,
+    // 128-byte swizzled as the MMAs read them; a bad page is read past the
+    // map's end (zeros).  Once a tile has landed, the token rows past the
+    // sequence are cleared (thread half gh: planes 2gh, 2gh+1 and half the RoPE
+    // plane of row t), and the tile is handed over.
     const int t = tid >> 1, gh = tid & 1;
-    auto issue = [&](int i) {
-      uint8_t* A = sA + (i % NB) * ABUF;
+    int issued = 0;
+    auto issue = [&](int i) {  // thread 0
+      const int buf = i % NB;
       const long long page = s_pages[i];
       const bool ok_p = page >= 0 && page < a.num_pages;
-      if (!ok_p && tid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
-      const bool okt = ok_p && (sw.page_begin + i) * kPageTokens + t < L;
-      const uint8_t* row = a.pool + (ok_p ? page : 0) * (long long)G.page_bytes + t * G.content_row;
+      if (!ok_p) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+      const int y = ok_p ? (int)(page * kPageTokens) : -kPageTokens;
+      const uint32_t dst = tc::su32(sA + buf * ABUF), tb = bar(kBarTFull + buf);
+      expect_tx(tb, 5 * kPlane);
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = 2 * gh + jj;
-        uint8_t* p1 = A + j * kPlane;
-#pragma unroll
-        for (int c2 = 0; c2 < 8; ++c2) {
-          const int c = c2 ^ (gh << 2);  // the token's two threads walk the chunks in different orders
-          uint8_t* dst = p1 + tc::sw_chunk(t, c);
-          if (okt) {
-            cp_async16(dst, row + 128 * (4 * r + j) + 16 * c);
-          } else {
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
-#pragma unroll
-      for (int k2 = 0; k2 < 2; ++k2) {
-        const int c = 4 * r + 2 * gh + k2;
-        uint8_t* dst = A + 4 * kPlane + tc::sw_chunk(t, c);
-        if (okt) {
-          cp_async16(dst, row + 1024 + 16 * c);
-        } else {
-          *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      for (int j = 0; j < 4; ++j) tma_load_2d(dst + j * kPlane, &tmap, 64 * (4 * r + j), y, tb);
+      tma_load_2d(dst + 4 * kPlane, &tmap, kLatent, y, tb);
     };
-    for (int i = 0; i < NB - 1; ++i) {
-      if (i < n_pk) {
-        issue(i);
-      } else {
-        asm volatile("cp.async.commit_group;" ::: "memory");
-      }
+    if (tid == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+      for (; issued < min(NB - 1, n_pk); ++issued) issue(issued);
     }
+    int consumed = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i % NB;
-      // this tile's copies are complete (the NB - 2 later groups may still run)
-      asm volatile("cp.async.wait_group %0;" ::"n"(kNBF - 2) : "memory");
+      if (!wait(bar(kBarTFull + buf), (i / NB) & 1, abort_flag, a.err, a.wait_cycles)) break;
+      consumed = i + 1;
+      const long long page = s_pages[i];
+      const bool okt = page >= 0 && page < a.num_pages && (sw.page_begin + i) * kPageTokens + t < L;
+      if (!okt) {
+        uint8_t* A = sA + buf * ABUF;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(A + (2 * gh + jj) * kPlane + tc::sw_chunk(t, c)) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(A + 4 * kPlane + tc::sw_chunk(t, 4 * gh + c)) = make_uint4(0, 0, 0, 0);
+      }
       tc::fence_async_smem();
-      const bool okt = i < n_pk && s_pages[i] >= 0 && s_pages[i] < a.num_pages &&
-                       (sw.page_begin + i) * kPageTokens + t < L;
       uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
       mk = (mk | (mk >> 1)) & 0x33333333u;
       mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
@@ -503,12 +512,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool free_ok =
             i < 1 || wait(bar(kBarAFree + (i - 1) % NB), ((i - 1) / NB) & 1, abort_flag, a.err, a.wait_cycles);
         if (!__all_sync(0xffffffffu, free_ok)) break;
-        issue(nxt);
-      } else {
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (tid == 0) {
+          issue(nxt);
+          issued = nxt + 1;
+        }
       }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // copies issued but not waited for (an early exit) land before the CTA leaves
+    if (tid == 0)
+      for (int i = consumed; i < issued; ++i) drain_wait(bar(kBarTFull + i % NB), (i / NB) & 1, a.wait_cycles);
   } else if (warp < 4) {
     // ---------------- unpack: token t of every tile; thread half gh takes
     // content groups 2gh, 2gh+1 and RoPE words 4r+2gh, 4r+2gh+1 (16 channels)
@@ -1113,15 +1125,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace wide
 
+// The driver's tensor-map encoder, looked up once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
 cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stream) {
   const int smem = wide::kSmem + 1024;
-  void (*kern)(DecodeArgs) = cbits == 4   ? wide::decode_wide_kernel<4>
-                             : cbits == 2 ? wide::decode_wide_kernel<2>
-                                          : wide::decode_wide_kernel<16>;
+  void (*kern)(DecodeArgs, CUtensorMap) = cbits == 4   ? wide::decode_wide_kernel<4>
+                                          : cbits == 2 ? wide::decode_wide_kernel<2>
+                                                       : wide::decode_wide_kernel<16>;
   const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
+  // bf16 pages: a 2-D map of the pool, [pages * 64 token rows][576 channels],
+  // boxes of 64 x 64 (one plane) with the 128-byte swizzle of the MMA operands
+  CUtensorMap tmap;
+  memset(&tmap, 0, sizeof(tmap));
+  if (cbits == 16) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)a.num_pages * kPageTokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+    const cuuint32_t box[2] = {64, kPageTokens};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(a.pool), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   dim3 grid(2 * a.total_splits, a.H / wide::kRows), block(wide::kThreads);
-  kern<<<grid, block, smem, stream>>>(a);
+  kern<<<grid, block, smem, stream>>>(a, tmap);
   return cudaGetLastError();
 }
 
