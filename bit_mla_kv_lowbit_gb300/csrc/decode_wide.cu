@@ -1,7 +1,7 @@
 // Split-KV low-bit MLA decode for query rows in blocks of 128 per sequence
 // (128 heads, n_q query blocks of 128 / n_q heads, or n_q blocks of 128 heads)
 // on the 5th-generation tensor cores, one 2-CTA cluster per (split, 128-row
-// block), for packed caches.
+// block), for packed caches and (a template variant) bf16 pages.
 //
 // Same arithmetic as decode.cu (QuantMLA, Abstract and Figure 8 caption:
 // exact integer codes on the tensor cores, per-group fp16 scale and min, one
@@ -35,10 +35,16 @@
 //   (128 x 256 fp32) stays in tensor memory for the whole split and is
 //   rescaled only when a row's running max grows by more than kLazy.
 //
+// bf16 pages need none of the scale machinery: the planes are the cache's own
+// bf16 rows (one per group, no s_lo planes, no min terms), loaded by the
+// tensor-memory accelerator into a 4-deep ring; QK and PV run as bf16 MMAs
+// with P in bf16 high and low parts.
+//
 // Warp roles (448 threads, one CTA per SM):
 //   warps 0-3   unpack: two threads per token of the tile (one per half of the
 //               CTA's groups); the next tile's bytes are loaded into registers
-//               while a plane buffer drains;
+//               while a plane buffer drains (bf16 pages: one thread issues the
+//               tensor copies, the warps clear rows past the sequence);
 //   warps 4-11  softmax: TMEM lane quadrant w & 3 (32 rows), token half
 //               (w - 4) >> 2 (32 tokens);
 //   warp 12     QK issue (one lane) and the TMEM allocation;
