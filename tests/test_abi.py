@@ -209,3 +209,20 @@ def test_plan_spreads_work_over_full_waves():
     assert pkg.decode_plan(lay, 128, [1048576] * 4, num_sms=152)[:2] == (532, 124)
     # rotation runs on the 16-row kernel: the 64-page cap
     assert pkg.decode_plan(pkg.layout(4, 4, rotate=True), 128, [131072] * 4, num_sms=152)[1] <= 64
+
+
+def test_plan_takes_more_waves_when_they_are_faster():
+    # 32 sequences of 4K-16K tokens at 128 heads: the fewest waves (one) need
+    # 96-unit chunks, because each sequence's splits round up; two waves of
+    # 43-unit chunks take about waves * (chunk + 3) = 92 units against 99, so
+    # the planner takes two.  The 128K headline keeps its single wave.
+    from workloads import synthetic as syn
+    lay = pkg.layout(4, 4)
+    lens = [int(x) for x in syn.sequence_lengths(syn.get("v3_c4r4"))]
+    total, chunk, _ = pkg.decode_plan(lay, 128, lens, num_sms=152)
+    waves = -(-total * 2 // 152)
+    assert (total, chunk, waves) == (151, 43, 2)
+    one_wave = sum(_expected_splits(L, True, 96) for L in lens)
+    assert one_wave * 2 <= 152 and sum(_expected_splits(L, True, 95) for L in lens) * 2 > 152
+    assert waves * (chunk + 3) * 20 < 1 * (96 + 3) * 19
+    assert pkg.decode_plan(lay, 128, [131072] * 4, num_sms=152)[:2] == (76, 109)
