@@ -40,13 +40,18 @@
 // tensor-memory accelerator into a 4-deep ring; QK and PV run as bf16 MMAs
 // with P in bf16 high and low parts.
 //
+// Packed caches run 48-token tiles in a 3-deep ring of plane sets (s_hi and
+// s_lo planes, 60 KB a set), so the unpack of a tile waits for the PV of the
+// tile three back; bf16 pages run 64-token tiles in a 4-deep ring.
+//
 // Warp roles (448 threads, one CTA per SM):
 //   warps 0-3   unpack: two threads per token of the tile (one per half of the
-//               CTA's groups); the next tile's bytes are loaded into registers
-//               while a plane buffer drains (bf16 pages: one thread issues the
-//               tensor copies, the warps clear rows past the sequence);
+//               CTA's groups; warps 0-2 for 48-token tiles); the next tile's
+//               bytes are loaded into registers while a plane buffer drains
+//               (bf16 pages: one thread issues the tensor copies, the warps
+//               clear rows past the sequence);
 //   warps 4-11  softmax: TMEM lane quadrant w & 3 (32 rows), token half
-//               (w - 4) >> 2 (32 tokens);
+//               (w - 4) >> 2 (24 or 32 tokens);
 //   warp 12     QK issue (one lane) and the TMEM allocation;
 //   warp 13     PV issue (one lane): a tile's PV starts as soon as its P is in
 //               tensor memory, whatever the next tile's QK is waiting for.
@@ -68,71 +73,85 @@ using namespace tc;
 
 constexpr int kRows = 128;
 constexpr int kThreads = 448;
-constexpr int kUnpackThreads = 128;
 constexpr int kSoftWarp0 = 4;
 constexpr int kSoftThreads = 256;
 constexpr int kIssuerWarp = 12;      // QK
 constexpr int kPvWarp = 13;          // PV
-constexpr int kTW = 32;                 // tokens of a tile per softmax warp
-constexpr int kNB = 2;                  // plane-set ring depth (tiles)
-constexpr int kNBF = 4;                 // the same for bf16 pages (half the planes per tile)
 constexpr int kMaxOwn = 5;              // QK groups of a CTA
-constexpr int kPlane = 64 * 128;        // 64 tokens x 64 fp16 (128-byte rows)
-constexpr int kABuf = 2 * kMaxOwn * kPlane;  // s_hi planes of the 5 groups, then s_lo planes
 constexpr int kQBlock = kRows * 128;    // 128 rows x 64 fp16
 constexpr float kLazy = 8.0f;           // log2 units
 constexpr float kShiftAbove = 32768.f;  // |s c| bound beyond which a token's planes are scaled by 2^-4
 constexpr int kQPitch = 41;             // uint4 per row of the q staging (5 groups x 8 + 1)
 constexpr int kOPitch = 260;            // floats per row of the output staging (16-byte stores at 4 wavefronts)
-
-// shared memory (bytes, from a 1 KB aligned base)
-constexpr int kOffA = 0;                                     // [kNB] plane sets
-constexpr int kOffQR = kOffA + kNB * kABuf;                  // RoPE q block
-// exchange buffer: [2 token halves][8 chunks of 4 tokens][128 rows] float4, so
-// that a warp's 16-byte stores (and loads) of one chunk are 512 contiguous bytes
-constexpr int kOffX = kOffQR + kQBlock;
-constexpr int kOffMeta = kOffX + 2 * 8 * kRows * 16;         // [kNB][5][64] fp32 m'
-constexpr int kOffShift = kOffMeta + kNB * kMaxOwn * 64 * 4; // [kNB][64] fp32 token factor
-constexpr int kOffValid = kOffShift + kNB * 64 * 4;          // [kNBF][4] 16-token masks
-constexpr int kOffMax = kOffValid + kNBF * 4 * 4;            // [2][2][128] fp32
-constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
-constexpr int kOffPages = kOffScan + 32 * 4;                 // [128] page ids of the split
-constexpr int kOffBar = kOffPages + 128 * 4;
 constexpr int kNumBars = 33;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
-constexpr int kSmem = kOffMisc + 64;
-static_assert(kOffQR % 1024 == 0 && kPlane % 1024 == 0, "swizzled operands need 1 KB alignment");
-static_assert(kOffBar % 8 == 0, "mbarrier alignment");
-static_assert(kSmem + 1024 <= 227 * 1024, "shared memory budget (with 1 KB alignment slack)");
-static_assert(kRows * kOPitch * 4 <= kNB * kABuf, "output staging fits the plane buffers");
-static_assert(kRows * kQPitch * 16 <= kNB * kABuf, "q staging fits the plane buffers");
+constexpr int kMaxSmem = 227 * 1024;
+
+// Tile geometry and shared-memory layout (bytes, from a 1 KB aligned base) by
+// layout.  Packed caches use 48-token tiles, so that three sets of s_hi and
+// s_lo planes fit (a tile's planes live from its unpack to the end of its PV,
+// and the ring depth divides that lifetime); bf16 pages use 64-token tiles
+// (one page, one tensor-copy box per plane) in a 4-deep ring of s_hi-only sets.
+template <int CB>
+struct Geo {
+  static constexpr bool kBF = CB == 16;
+  static constexpr int kTok = kBF ? 64 : 48;              // tokens per tile
+  static constexpr int kTW = kTok / 2;                    // tokens of a tile per softmax warp
+  static constexpr int kNB = kBF ? 4 : 3;                 // plane-set ring depth
+  static constexpr int kPlane = kTok * 128;               // kTok tokens x 64 fp16 (128-byte rows)
+  static constexpr int kABuf = (kBF ? 1 : 2) * kMaxOwn * kPlane;  // s_hi planes, then s_lo planes
+  static constexpr int kXChunks = kTW / 4;                // 4-token chunks of a softmax warp
+  static constexpr int kOffA = 0;                         // [kNB] plane sets
+  static constexpr int kOffQR = kOffA + kNB * kABuf;      // RoPE q block
+  // exchange buffer: [2 token halves][kXChunks chunks of 4 tokens][128 rows]
+  // float4, so that a warp's 16-byte stores (and loads) of one chunk are 512
+  // contiguous bytes
+  static constexpr int kOffX = kOffQR + kQBlock;
+  static constexpr int kOffMeta = kOffX + 2 * kXChunks * kRows * 16;  // [kNB][4][kTok] fp32 m' (content groups)
+  static constexpr int kOffShift = kOffMeta + kNB * 4 * kTok * 4;     // [kNB][kTok] token factor
+  static constexpr int kOffValid = kOffShift + kNB * kTok * 4;        // [kNB][4] 16-token masks
+  static constexpr int kOffMax = kOffValid + kNB * 4 * 4;             // [2][2][128] fp32
+  static constexpr int kOffScan = kOffMax + 2 * 2 * kRows * 4;        // [32] int
+  static constexpr int kOffPages = kOffScan + 32 * 4;                 // [128] page ids of the split
+  static constexpr int kOffBar = kOffPages + 128 * 4;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
+  static constexpr int kSmem = kOffMisc + 64;
+  static constexpr int kLaunch = kSmem + 1024;  // the layout plus room to align the base to 1 KB
+  static_assert(kOffQR % 1024 == 0 && kPlane % 1024 == 0 && kABuf % 1024 == 0,
+                "swizzled operands need 1 KB alignment");
+  static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+  static_assert(kLaunch <= kMaxSmem, "shared memory budget");
+  static_assert(kRows * kOPitch * 4 <= kNB * kABuf, "output staging fits the plane buffers");
+  static_assert(kRows * kQPitch * 16 <= kNB * kABuf, "q staging fits the plane buffers");
+  static_assert(kTok % 16 == 0 && kTW % 8 == 0, "MMA N and P k-steps");
+};
 
 // mbarriers
-constexpr int kBarAFull = 0;    // [kNB or kNBF] count 128 (unpack or copy threads)
-constexpr int kBarAFree = 4;    // [kNB or kNBF] count 1 (issuer commit after the tile's PV)
+constexpr int kBarAFull = 0;    // [kNB] count 2 kTok (unpack or copy threads)
+constexpr int kBarAFree = 4;    // [kNB] count 1 (issuer commit after the tile's PV)
 constexpr int kBarDFull = 8;    // count 1: the tile's QK is complete
 constexpr int kBarDFree = 9;    // count 256: the softmax warps have read it
 constexpr int kBarPFull = 10;   // count 256: P of the tile is in tensor memory
 constexpr int kBarPFree = 11;   // count 1: the tile's PV is complete
 constexpr int kBarFlush = 12;   // count 2: final drain of both issuers
-constexpr int kBarXFull = 13;   // [8] per softmax warp w: count 1 + 4 KB of transactions, the peer's
+constexpr int kBarXFull = 13;   // [8] per softmax warp w: count 1 + the partial's bytes, the peer's
                                 //     warp w has written its partial logits into my buffer
 constexpr int kBarXFree = 21;   // [8] per softmax warp w: count 1, the peer's warp w has read its buffer
-constexpr int kBarTFull = 29;   // [kNBF] bf16 pages: count 1 + 40 KB of tensor-copy transactions
+constexpr int kBarTFull = 29;   // [kNB] bf16 pages: count 1 + 40 KB of tensor-copy transactions
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;     // [4 groups][64 channels] fp32
-constexpr uint32_t kColD = 256;   // [64 tokens] fp32 QK accumulator
-constexpr uint32_t kColP = 320;   // [hi 32 | lo 32] fp16 pairs: P of 64 tokens
+constexpr uint32_t kColD = 256;   // [kTok tokens] fp32 QK accumulator
+constexpr uint32_t kColP = 320;   // [hi kTok/2 | lo kTok/2] fp16 pairs: P of kTok tokens
 constexpr uint32_t kColQ = 384;   // [4 content groups][32] fp16 pairs: q
 constexpr uint32_t kTmemCols = 512;
 
-// v[t] *= f[t] for the 32 tokens of a softmax warp's half tile (the factor 16
+// v[t] *= f[t] for the tokens of a softmax warp's half tile (the factor 16
 // of tokens whose planes were stored scaled by 2^-4); called only for tiles
 // that hold such a token.
-__device__ __forceinline__ void scale_by_token(float (&v)[kTW], const float4* f4) {
+template <int N>
+__device__ __forceinline__ void scale_by_token(float (&v)[N], const float4* f4) {
 #pragma unroll
-  for (int t4 = 0; t4 < kTW / 4; ++t4) {
+  for (int t4 = 0; t4 < N / 4; ++t4) {
     const float4 f = f4[t4];
     v[4 * t4] *= f.x;
     v[4 * t4 + 1] *= f.y;
@@ -263,27 +282,31 @@ __device__ __forceinline__ int chan_at(int p, bool tb) { return tc::chan_of_pos(
 template <int CB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_wide_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
-  constexpr bool kBF = CB == 16;     // bf16 pages: planes are the values themselves
-  constexpr int NB = kBF ? kNBF : kNB;           // plane-set ring depth
-  constexpr int ABUF = kBF ? kABuf / 2 : kABuf;  // bytes per plane set (bf16: no s_lo planes)
+  using GG = Geo<CB>;
+  constexpr bool kBF = GG::kBF;      // bf16 pages: planes are the values themselves
+  constexpr int NB = GG::kNB;        // plane-set ring depth
+  constexpr int ABUF = GG::kABuf;    // bytes per plane set (bf16: no s_lo planes)
+  constexpr int TOK = GG::kTok;      // tokens per tile
+  constexpr int TW = GG::kTW;        // tokens of a tile per softmax warp
+  constexpr int PL = GG::kPlane;     // bytes per plane
   constexpr bool kTypeB = CB == 2;
   constexpr PageGeom G = page_geom(CB);
   constexpr float kCentreC = kTypeB ? float(kCentre2) : float(kCentre4);
   constexpr float kCmaxC = kTypeB ? 2.f : 8.f;  // largest |code - centre| of a content group
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::su32(smem_raw) & 1023)) & 1023);
-  uint8_t* sA = smem + kOffA;
-  uint8_t* sQR = smem + kOffQR;
-  float* sX = reinterpret_cast<float*>(smem + kOffX);
-  float* sMeta = reinterpret_cast<float*>(smem + kOffMeta);
-  float* sShift = reinterpret_cast<float*>(smem + kOffShift);
-  uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + kOffValid);
-  float* sMax = reinterpret_cast<float*>(smem + kOffMax);
-  int* scan = reinterpret_cast<int*>(smem + kOffScan);
-  int* s_pages = reinterpret_cast<int*>(smem + kOffPages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  uint8_t* sA = smem + GG::kOffA;
+  uint8_t* sQR = smem + GG::kOffQR;
+  float* sX = reinterpret_cast<float*>(smem + GG::kOffX);
+  float* sMeta = reinterpret_cast<float*>(smem + GG::kOffMeta);
+  float* sShift = reinterpret_cast<float*>(smem + GG::kOffShift);
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + GG::kOffValid);
+  float* sMax = reinterpret_cast<float*>(smem + GG::kOffMax);
+  int* scan = reinterpret_cast<int*>(smem + GG::kOffScan);
+  int* s_pages = reinterpret_cast<int*>(smem + GG::kOffPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GG::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GG::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GG::kOffMisc + 4);
   auto bar = [&](int i) { return tc::su32(&bars[i]); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -305,14 +328,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const SplitWork sw = split_work(L, split, a.chunk_pages, !kBF);
   const int n_pk = sw.n_pages;
+  // tiles of the split's run of paged tokens (packed: 48-token tiles over its
+  // n_pk pages, the last one ragged), then tiles of its protected tokens
+  const int n_pt = (n_pk * kPageTokens + TOK - 1) / TOK;
   const int bf_first = 64 * sw.bf_begin;
   const int bf_end = min(sw.n_tok, 64 * (sw.bf_begin + sw.n_bf));
-  const int n_tiles = n_pk + max(0, (bf_end - bf_first + 63) / 64);
+  const int n_tiles = n_pt + max(0, (bf_end - bf_first + TOK - 1) / TOK);
 
   // ---- set-up: barriers, TMEM, page ids, RoPE q block
   if (tid == 0) {
-    for (int i = 0; i < kNBF; ++i) {
-      tc::bar_init(bar(kBarAFull + i), kUnpackThreads);
+    for (int i = 0; i < NB; ++i) {
+      tc::bar_init(bar(kBarAFull + i), 2 * TOK);
       tc::bar_init(bar(kBarAFree + i), 1);
       tc::bar_init(bar(kBarTFull + i), 1);
     }
@@ -461,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < 4 && kBF) {
     // ---------------- copy (bf16 pages): thread 0 loads each tile's five
     // planes (the CTA's four content groups and the RoPE group, 64 tokens x 64
-    // channels each) with the tensor-memory accelerator, kNBF - 1 tiles ahead,
+    // channels each) with the tensor-memory accelerator, NB - 1 tiles ahead,
     // 128-byte swizzled as the MMAs read them; a bad page is read past the
     // map's end (zeros).  Once a tile has landed, the token rows past the
     // sequence are cleared (thread half gh: planes 2gh, 2gh+1 and half the RoPE
@@ -475,10 +501,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok_p) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
       const int y = ok_p ? (int)(page * kPageTokens) : -kPageTokens;
       const uint32_t dst = tc::su32(sA + buf * ABUF), tb = bar(kBarTFull + buf);
-      expect_tx(tb, 5 * kPlane);
+      expect_tx(tb, 5 * PL);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tma_load_2d(dst + j * kPlane, &tmap, 64 * (4 * r + j), y, tb);
-      tma_load_2d(dst + 4 * kPlane, &tmap, kLatent, y, tb);
+      for (int j = 0; j < 4; ++j) tma_load_2d(dst + j * PL, &tmap, 64 * (4 * r + j), y, tb);
+      tma_load_2d(dst + 4 * PL, &tmap, kLatent, y, tb);
     };
     if (tid == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
@@ -497,10 +523,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(A + (2 * gh + jj) * kPlane + tc::sw_chunk(t, c)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(A + (2 * gh + jj) * PL + tc::sw_chunk(t, c)) = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(A + 4 * kPlane + tc::sw_chunk(t, 4 * gh + c)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(A + 4 * PL + tc::sw_chunk(t, 4 * gh + c)) = make_uint4(0, 0, 0, 0);
       }
       tc::fence_async_smem();
       uint32_t mk = __ballot_sync(0xffffffffu, okt) & 0x55555555u;
@@ -527,24 +553,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // copies issued but not waited for (an early exit) land before the CTA leaves
     if (tid == 0)
       for (int i = consumed; i < issued; ++i) drain_wait(bar(kBarTFull + i % NB), (i / NB) & 1, a.wait_cycles);
-  } else if (warp < 4) {
-    // ---------------- unpack: token t of every tile; thread half gh takes
-    // content groups 2gh, 2gh+1 and RoPE words 4r+2gh, 4r+2gh+1 (16 channels)
+  } else if (warp < 4 && (tid >> 1) < TOK) {
+    // ---------------- unpack: token t of every tile (warps 0-2: 48 tokens);
+    // thread half gh takes content groups 2gh, 2gh+1 and RoPE words 4r+2gh,
+    // 4r+2gh+1 (16 channels).  Tile i holds tokens 48i .. 48i+47 of the
+    // split's run of pages, so a tile can span two pages.
     const int t = tid >> 1, gh = tid & 1;
     uint4 nc[4];
     uint2 nr = make_uint2(0, 0);
     uint32_t nm[3];
     bool n_ok = false, n_okt = false;
     auto fetch = [&](int i) {
-      const int page_idx = sw.page_begin + i;
-      const long long page = s_pages[i];
-      const int pos = page_idx * kPageTokens + t;
-      n_ok = page >= 0 && page < a.num_pages;
-      if (!n_ok && tid == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+      const int rel = TOK * i + t;  // token of the split's run of pages
+      const int pi = rel >> 6, row = rel & (kPageTokens - 1);
+      const bool in_run = pi < n_pk;
+      const long long page = in_run ? s_pages[pi] : 0;
+      const int pos = (sw.page_begin + pi) * kPageTokens + row;
+      const bool page_ok = page >= 0 && page < a.num_pages;
+      if (in_run && !page_ok && gh == 0) set_error(a.err, MLA_LOWBIT_DEV_BAD_PAGE);
+      n_ok = in_run && page_ok;
       n_okt = n_ok && pos >= kSink && pos < L - kLocal;
       const uint8_t* pb = a.pool + (n_ok ? page : 0) * (long long)G.page_bytes;
-      const uint8_t* crow = pb + G.content_off + t * G.content_row;
-      const uint8_t* mrow = pb + G.meta_off + t * G.meta_row;
+      const uint8_t* crow = pb + G.content_off + row * G.content_row;
+      const uint8_t* mrow = pb + G.meta_off + row * G.meta_row;
 #pragma unroll
       for (int k = 0; k < 4; ++k) nc[k] = make_uint4(0, 0, 0, 0);
       nr = make_uint2(0, 0);
@@ -564,7 +595,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             nc[k] = gh ? make_uint4(v.z, v.w, v.x, v.y) : v;
           }
         }
-        nr = *reinterpret_cast<const uint2*>(pb + G.rope_off + t * G.rope_row + 16 * r + 8 * gh);
+        nr = *reinterpret_cast<const uint2*>(pb + G.rope_off + row * G.rope_row + 16 * r + 8 * gh);
       }
       if (n_okt) {
         nm[0] = *reinterpret_cast<const uint32_t*>(mrow + 4 * (4 * r + 2 * gh));
@@ -572,17 +603,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         nm[2] = *reinterpret_cast<const uint32_t*>(mrow + 32);
       }
     };
-    if (n_pk > 0) fetch(0);
+    if (n_pt > 0) fetch(0);
     for (int i = 0; i < n_tiles; ++i) {
-      const int buf = i % kNB;
+      const int buf = i % NB;
       uint4 cc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) cc[k] = nc[k];
       const uint2 rr = nr;
       const uint32_t mw0 = nm[0], mw1 = nm[1], mw2 = nm[2];
       const bool okt_cur = n_okt;
-      if (i + 1 < n_pk) fetch(i + 1);  // in flight while the buffer drains
-      const bool packed = i < n_pk;
+      if (i + 1 < n_pt) fetch(i + 1);  // in flight while the buffer drains
+      const bool packed = i < n_pt;
       // What needs only this tile's metadata is done before the buffer is
       // free: the token factor, the scale parts, m', the min-term chunks, the
       // RoPE codes and the validity mask.
@@ -631,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) rc[k] = 0u;
       }
-      const bool okt = packed ? okt_cur : bf_first + (i - n_pk) * 64 + t < bf_end;
+      const bool okt = packed ? okt_cur : bf_first + (i - n_pt) * TOK + t < bf_end;
       // validity of the warp's 16 tokens (lanes 2k and 2k+1 hold token k);
       // bit 31: some token of the 16 has its planes scaled by 2^-4
       const bool any_shift = __any_sync(0xffffffffu, shift);
@@ -640,21 +671,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mk = (mk | (mk >> 2)) & 0x0F0F0F0Fu;
       mk = (mk | (mk >> 4)) & 0x00FF00FFu;
       mk = (mk | (mk >> 8)) & 0x0000FFFFu;
-      // the buffer: free once the PV of tile i - kNB is complete (the lanes of
+      // the buffer: free once the PV of tile i - NB is complete (the lanes of
       // a warp leave together)
-      const bool free_ok = i < kNB || wait(bar(kBarAFree + buf), ((i / kNB) - 1) & 1, abort_flag, a.err, a.wait_cycles);
+      const bool free_ok = i < NB || wait(bar(kBarAFree + buf), ((i / NB) - 1) & 1, abort_flag, a.err, a.wait_cycles);
       if (!__all_sync(0xffffffffu, free_ok)) break;
-      uint8_t* A = sA + buf * kABuf;
-      float* meta = sMeta + buf * kMaxOwn * 64;
+      uint8_t* A = sA + buf * ABUF;
+      float* meta = sMeta + buf * 4 * TOK;
       if (packed) {
-        if (gh == 0) sShift[buf * 64 + t] = shift ? 16.f : 1.f;
+        if (gh == 0) sShift[buf * TOK + t] = shift ? 16.f : 1.f;
         // the thread's two content groups in a rolled loop (code size): the
         // group in hand is always cc[0..] with hiA/loA/mqA, shifted down afterwards
 #pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * gh + jj;
-          uint8_t* p1 = A + j * kPlane;
-          uint8_t* p2 = A + (kMaxOwn + j) * kPlane;
+          uint8_t* p1 = A + j * PL;
+          uint8_t* p2 = A + (kMaxOwn + j) * PL;
           // the token's two threads write the same positions of planes 8 KB
           // apart (same banks): the second one walks the chunks in another
           // order, so that their stores never meet in one bank
@@ -690,7 +721,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
           }
-          meta[j * 64 + t] = mqA;
+          meta[j * TOK + t] = mqA;
           mqA = mqB;
           hiA = hiB;
           loA = loB;
@@ -703,8 +734,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         {
           // RoPE words 4r + 2gh, 4r + 2gh + 1 -> chunks of the same index
-          uint8_t* p1 = A + 4 * kPlane;
-          uint8_t* p2 = A + (kMaxOwn + 4) * kPlane;
+          uint8_t* p1 = A + 4 * PL;
+          uint8_t* p2 = A + (kMaxOwn + 4) * PL;
 #pragma unroll
           for (int k2 = 0; k2 < 2; ++k2) {
             const int c = 4 * r + 2 * gh + k2;
@@ -719,14 +750,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         // protected tokens: bf16 values as the s_hi plane, zero s_lo plane, min 0
-        const int idx = bf_first + (i - n_pk) * 64 + t;
+        const int idx = bf_first + (i - n_pt) * TOK + t;
         const uint16_t* rp = nullptr;
         if (okt) {
           const int pos = bf16_pos(sw, idx);
           rp = pos < kSink ? a.sink + ((long long)b * kSink + pos) * kDim
                            : a.recent + ((long long)b * kLocal + pos % kLocal) * kDim;
         }
-        if (gh == 0) sShift[buf * 64 + t] = 1.f;
+        if (gh == 0) sShift[buf * TOK + t] = 1.f;
         // 16-channel blocks: 4 per content group (2 groups), then RoPE block 2r + gh
 #pragma unroll 1
         for (int blk = 0; blk < 9; ++blk) {
@@ -734,8 +765,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int cc16 = blk < 8 ? (blk & 3) : 2 * r + gh;
           const int g = j < 4 ? 4 * r + j : 8;
           const bool tb = j < 4 && kTypeB;
-          uint8_t* p1 = A + j * kPlane;
-          uint8_t* p2 = A + (kMaxOwn + j) * kPlane;
+          uint8_t* p1 = A + j * PL;
+          uint8_t* p2 = A + (kMaxOwn + j) * PL;
           uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
           if (rp) {
             v0 = reinterpret_cast<const uint4*>(rp + g * 64 + 16 * cc16)[0];
@@ -758,12 +789,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(p2 + tc::sw_chunk(t, c)) = make_uint4(0, 0, 0, 0);
           }
         }
-        meta[(2 * gh) * 64 + t] = 0.f;
-        meta[(2 * gh + 1) * 64 + t] = 0.f;
+        meta[(2 * gh) * TOK + t] = 0.f;
+        meta[(2 * gh + 1) * TOK + t] = 0.f;
         // no min terms: zero min-term k-steps
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2)
-          *reinterpret_cast<uint4*>(A + 4 * kPlane + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
+          *reinterpret_cast<uint4*>(A + 4 * PL + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
               make_uint4(0, 0, 0, 0);
       }
       if (lane == 0) sMask[buf * 4 + warp] = mk | (any_shift ? 0x80000000u : 0u);
@@ -777,7 +808,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // logits; PV of each tile once its P is in tensor memory.  Each issuer
     // commits its own MMAs (a commit tracks the issuing thread's operations).
     if (lane == 0) {
-      const uint32_t id_qk = tc::idesc(128, 64, 0, 0);    // A K-major, B K-major
+      const uint32_t id_qk = tc::idesc(128, TOK, 0, 0);   // A K-major, B K-major
       // the same shape with bf16 A and B (bits 7-9, 10-12: format 1) for the
       // min-term k-steps
       const uint32_t id_min = id_qk | (1u << 7) | (1u << 10);
@@ -791,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // descriptors differ only in their start address (16-byte units in the
       // low bits, no carry for shared-memory addresses)
       const uint64_t kq0 = tc::desc(tc::su32(sA), 16, 1024);
-      const uint64_t kp0 = tc::desc(tc::su32(sA), kPlane, 1024);
+      const uint64_t kp0 = tc::desc(tc::su32(sA), PL, 1024);
       const uint64_t qr0 = tc::desc(tc::su32(sQR), 16, 1024);
       // (the issue loops are unrolled: with the descriptors folded to
       // constants an MMA issues every ~46 cycles, against ~60 from a rolled loop)
@@ -807,10 +838,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int ks = 0; ks < 4; ++ks) {
               const uint32_t qa = tmem + kColQ + 32 * j + 8 * ks;
               if constexpr (kBF) {  // bf16 q and values: one product, exact in fp32
-                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_min, (j | ks) != 0);
+                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * PL + 32 * ks) >> 4), id_min, (j | ks) != 0);
               } else {
-                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * kPlane + 32 * ks) >> 4), id_qk, (j | ks) != 0);
-                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * kPlane + 32 * ks) >> 4), id_qk, 1);
+                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)((j * PL + 32 * ks) >> 4), id_qk, (j | ks) != 0);
+                mma_tmem_a(tmem + kColD, qa, d + (uint64_t)(((kMaxOwn + j) * PL + 32 * ks) >> 4), id_qk, 1);
               }
             }
           }
@@ -820,12 +851,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int ks = 2 * r + k2;
             if constexpr (kBF) {
               tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                      d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+                      d + (uint64_t)((4 * PL + 32 * ks) >> 4), id_min, 1);
             } else {
               tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                      d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_qk, 1);
+                      d + (uint64_t)((4 * PL + 32 * ks) >> 4), id_qk, 1);
               tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                      d + (uint64_t)(((kMaxOwn + 4) * kPlane + 32 * ks) >> 4), id_qk, 1);
+                      d + (uint64_t)(((kMaxOwn + 4) * PL + 32 * ks) >> 4), id_qk, 1);
             }
           }
           // the min terms: the other rank's RoPE k-steps, in bf16
@@ -834,7 +865,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int k2 = 0; k2 < 2; ++k2) {
               const int ks = 2 * (1 - r) + k2;
               tc::mma(tmem + kColD, qr0 + (uint64_t)((32 * ks) >> 4),
-                      d + (uint64_t)((4 * kPlane + 32 * ks) >> 4), id_min, 1);
+                      d + (uint64_t)((4 * PL + 32 * ks) >> 4), id_min, 1);
             }
           }
           tc::commit(bar(kBarDFull));
@@ -847,11 +878,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc::tc_fence_after();
           const uint64_t d = kp0 + (uint64_t)(((k % NB) * ABUF) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
+          for (int ks = 0; ks < TOK / 16; ++ks) {
             // the four content groups' planes side by side: N = 256 channels
             const uint64_t b1 = d + (uint64_t)((2048 * ks) >> 4);
-            const uint64_t b2 = d + (uint64_t)((kMaxOwn * kPlane + 2048 * ks) >> 4);
-            const uint32_t phi = tmem + kColP + 8 * ks, plo = tmem + kColP + 32 + 8 * ks;
+            const uint64_t b2 = d + (uint64_t)((kMaxOwn * PL + 2048 * ks) >> 4);
+            const uint32_t phi = tmem + kColP + 8 * ks, plo = tmem + kColP + TOK / 2 + 8 * ks;
             if constexpr (kBF) {  // P in bf16 high and low parts, bf16 values
               mma_tmem_a(tmem + kColO, phi, b1, id_pv_bf, (k > 0 || ks > 0));
               mma_tmem_a(tmem + kColO, plo, b1, id_pv_bf, 1);
@@ -885,7 +916,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= kSoftWarp0) {
-    // ---------------- softmax: row h (TMEM lane), tokens kTW*th .. kTW*th+kTW-1
+    // ---------------- softmax: row h (TMEM lane), tokens TW*th .. TW*th+TW-1
     const int qd = warp & 3, th = (warp - kSoftWarp0) >> 2, h = 32 * qd + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
     const uint32_t x_peer = map_peer(tc::su32(sX), peer);
@@ -902,44 +933,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int done_tiles = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i % NB;
-      const bool packed_tile = i < n_pk;
-      const float* meta = sMeta + buf * kMaxOwn * 64 + kTW * th;
-      const float4* f4 = reinterpret_cast<const float4*>(sShift + buf * 64 + kTW * th);
-      float S[kTW];
+      const bool packed_tile = i < n_pt;
+      const float* meta = sMeta + buf * 4 * TOK + TW * th;
+      const float4* f4 = reinterpret_cast<const float4*>(sShift + buf * TOK + TW * th);
+      float S[TW];
       // partial logits of my groups: the accumulator (scaled back per token)
       // plus the min terms.  The unpack warps' metadata of this tile is read
       // after an acquire on its plane-ready barrier (complete by now: QK ran).
       if (ok) ok = wait(bar(kBarDFull), i & 1, abort_flag, a.err, a.wait_cycles);
       if (ok) ok = wait(bar(kBarAFull + buf), (i / NB) & 1, abort_flag, a.err, a.wait_cycles);
-      const uint32_t mk0 = sMask[buf * 4 + 2 * th], mk1 = sMask[buf * 4 + 2 * th + 1];
-      const bool shifted = ((mk0 | mk1) >> 31) != 0;  // some token's logit and P take a factor 16
-      uint32_t vmask = (mk0 & 0xFFFFu) | ((mk1 & 0xFFFFu) << 16);
+      uint64_t vm64 = 0;
+      uint32_t mk_or = 0;
+#pragma unroll
+      for (int w = 0; w < TOK / 16; ++w) {
+        const uint32_t mk = sMask[buf * 4 + w];
+        vm64 |= (uint64_t)(mk & 0xFFFFu) << (16 * w);
+        mk_or |= mk;
+      }
+      const bool shifted = (mk_or >> 31) != 0;  // some token's logit and P take a factor 16
+      constexpr uint32_t kAll = TW == 32 ? 0xFFFFFFFFu : (1u << TW) - 1u;
+      uint32_t vmask = (uint32_t)(vm64 >> (TW * th)) & kAll;
       ok = warp_all(ok);
       if (ok) {
         tc::tc_fence_after();
-        tmem_ld32(tl + kColD + kTW * th, S);
+        if constexpr (TW == 32) {
+          tmem_ld32(tl + kColD + TW * th, S);
+        } else {
+          tmem_ld24(tl + kColD + TW * th, S);
+        }
         tc::tc_fence_before();
         tc::bar_arrive(bar(kBarDFree));
         // the accumulator holds the min terms too (scaled like the planes)
         if (shifted) scale_by_token(S, f4);
       }
-      // exchange with the peer: my partial of my kTW tokens goes to the
+      // exchange with the peer: my partial of my TW tokens goes to the
       // peer's buffer (once the peer has read the previous tile's), the peer's
       // partial of the same tokens arrives in mine
       if (ok && i >= 1) ok = bar_wait_cluster(bar(kBarXFree + sw_idx), (i - 1) & 1, abort_flag, a.err, a.wait_cycles);
       if (ok) {
 #pragma unroll
-        for (int k = 0; k < kTW / 4; ++k)
-          st_async4(x_peer + (uint32_t)(((th * 8 + k) * kRows + h) * 16), S[4 * k], S[4 * k + 1],
+        for (int k = 0; k < TW / 4; ++k)
+          st_async4(x_peer + (uint32_t)(((th * (TW / 4) + k) * kRows + h) * 16), S[4 * k], S[4 * k + 1],
                     S[4 * k + 2], S[4 * k + 3], xfull_peer);
-        if (lane == 0) expect_tx(bar(kBarXFull + sw_idx), 32 * kTW * 4);
+        if (lane == 0) expect_tx(bar(kBarXFull + sw_idx), 32 * TW * 4);
         ok = wait(bar(kBarXFull + sw_idx), i & 1, abort_flag, a.err, a.wait_cycles);
       }
       if (ok) {
         const float4* src = reinterpret_cast<const float4*>(sX);
 #pragma unroll
-        for (int k = 0; k < kTW / 4; ++k) {
-          const float4 v = src[(th * 8 + k) * kRows + h];
+        for (int k = 0; k < TW / 4; ++k) {
+          const float4 v = src[(th * (TW / 4) + k) * kRows + h];
           S[4 * k] += v.x;
           S[4 * k + 1] += v.y;
           S[4 * k + 2] += v.z;
@@ -949,23 +992,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // validity, log2 scale, tile max over both halves.  In bf16 tiles the
       // row's query block also masks the last protected tokens.
       if (!packed_tile) {
-        const int lim = sw.n_tok - n_masked - (bf_first + (i - n_pk) * 64 + kTW * th);
-        vmask &= lim <= 0 ? 0u : lim >= kTW ? 0xFFFFFFFFu : (1u << lim) - 1u;
+        const int lim = sw.n_tok - n_masked - (bf_first + (i - n_pt) * TOK + TW * th);
+        vmask &= lim <= 0 ? 0u : lim >= TW ? kAll : (1u << lim) - 1u;
       } else if (kBF && n_masked > 0) {
         // bf16 pages hold the last tokens too: the row's query block does not
         // see the sequence's last n_masked of them
-        const int lim = L - n_masked - ((sw.page_begin + i) * kPageTokens + kTW * th);
-        vmask &= lim <= 0 ? 0u : lim >= kTW ? 0xFFFFFFFFu : (1u << lim) - 1u;
+        const int lim = L - n_masked - ((sw.page_begin + i) * kPageTokens + TW * th);
+        vmask &= lim <= 0 ? 0u : lim >= TW ? kAll : (1u << lim) - 1u;
       }
       // (the max of the raw logits, scaled once: the scale is positive and
       // rounding is monotonic, so this is the max of the scaled logits)
       float mx = -INFINITY;
-      if (vmask == 0xFFFFFFFFu) {
+      if (vmask == kAll) {
 #pragma unroll
-        for (int t = 0; t < kTW; ++t) mx = fmaxf(mx, S[t]);
+        for (int t = 0; t < TW; ++t) mx = fmaxf(mx, S[t]);
       } else {
 #pragma unroll
-        for (int t = 0; t < kTW; ++t) {
+        for (int t = 0; t < TW; ++t) {
           S[t] = ((vmask >> t) & 1u) ? S[t] : -INFINITY;
           mx = fmaxf(mx, S[t]);
         }
@@ -1005,7 +1048,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float mneg = m_run == -INFINITY ? 0.f : -m_run;
       float lsum = 0.f;
 #pragma unroll
-      for (int t = 0; t < kTW; ++t) {
+      for (int t = 0; t < TW; ++t) {
         S[t] = fast_exp2(fmaf(S[t], a.scale_log2, mneg));
         lsum += S[t];
       }
@@ -1016,10 +1059,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // after the fourth.
 #pragma unroll 1
       for (int j = 0; j < (kBF ? 0 : 4); ++j) {
-        const float4* m4 = reinterpret_cast<const float4*>(meta + j * 64);
+        const float4* m4 = reinterpret_cast<const float4*>(meta + j * TOK);
         float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int t4 = 0; t4 < kTW / 4; ++t4) {
+        for (int t4 = 0; t4 < TW / 4; ++t4) {
           const float4 mv = m4[t4];
           am[0] = fmaf(S[4 * t4], mv.x, am[0]);
           am[1] = fmaf(S[4 * t4 + 1], mv.y, am[1]);
@@ -1035,18 +1078,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // P (times each token's plane factor) as fp16 high and low parts
       if (ok) {
         tc::tc_fence_after();
-        uint32_t hi[kTW / 2], lo[kTW / 2];
+        uint32_t hi[TW / 2], lo[TW / 2];
         if (shifted) scale_by_token(S, f4);
 #pragma unroll
-        for (int t2 = 0; t2 < kTW / 2; ++t2) {
+        for (int t2 = 0; t2 < TW / 2; ++t2) {
           if constexpr (kBF) {
             split_trunc_bf16(S[2 * t2], S[2 * t2 + 1], hi[t2], lo[t2]);
           } else {
             split_trunc(S[2 * t2], S[2 * t2 + 1], hi[t2], lo[t2]);
           }
         }
-        tmem_st16_nowait(tl + kColP + (kTW / 2) * th, hi);
-        tmem_st16_nowait(tl + kColP + 32 + (kTW / 2) * th, lo);
+        if constexpr (TW == 32) {
+          tmem_st16_nowait(tl + kColP + (TW / 2) * th, hi);
+          tmem_st16_nowait(tl + kColP + TOK / 2 + (TW / 2) * th, lo);
+        } else {
+          tmem_st12_nowait(tl + kColP + (TW / 2) * th, hi);
+          tmem_st12_nowait(tl + kColP + TOK / 2 + (TW / 2) * th, lo);
+        }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc::tc_fence_before();
         tc::bar_arrive(bar(kBarPFull));
@@ -1146,7 +1194,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 cudaError_t launch_decode_wide(int cbits, const DecodeArgs& a, cudaStream_t stream) {
-  const int smem = wide::kSmem + 1024;
+  const int smem = cbits == 16 ? wide::Geo<16>::kLaunch : wide::Geo<4>::kLaunch;
   void (*kern)(DecodeArgs, CUtensorMap) = cbits == 4   ? wide::decode_wide_kernel<4>
                                           : cbits == 2 ? wide::decode_wide_kernel<2>
                                                        : wide::decode_wide_kernel<16>;

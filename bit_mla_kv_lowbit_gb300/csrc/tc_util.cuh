@@ -113,6 +113,36 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 24 consecutive columns of this thread's lane as an x16 and an x8 load (in
+// the order that keeps each naturally aligned: x8 first when the start is not
+// a multiple of 16), one wait.
+__device__ __forceinline__ void tmem_ld24(uint32_t taddr, float* v) {
+  uint32_t r[24];
+  const bool a16 = (taddr & 15u) == 0;
+  const uint32_t t16 = a16 ? taddr : taddr + 8, t8 = a16 ? taddr + 16 : taddr;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(t16));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                 "=r"(r[22]), "=r"(r[23])
+               : "r"(t8));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  if (a16) {
+#pragma unroll
+    for (int i = 0; i < 24; ++i) v[i] = __uint_as_float(r[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[16 + i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[8 + i] = __uint_as_float(r[i]);
+  }
+}
+
 // cp.async of 4, 8 or 16 bytes (global -> shared), one commit group per tile
 __device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes) {
   const uint32_t d = su32(dst);
@@ -185,6 +215,24 @@ __device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* 
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4_nowait(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+// 12 consecutive columns as an x8 and an x4 store, each naturally aligned
+// (the start is a multiple of 4).
+__device__ __forceinline__ void tmem_st12_nowait(uint32_t taddr, const uint32_t* v) {
+  if ((taddr & 7u) == 0) {
+    tmem_st8_nowait(taddr, v);
+    tmem_st4_nowait(taddr + 8, v + 8);
+  } else {
+    tmem_st4_nowait(taddr, v);
+    tmem_st8_nowait(taddr + 4, v + 4);
+  }
 }
 
 // 32 consecutive columns of this thread's lane, one wait.
