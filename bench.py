@@ -665,7 +665,10 @@ def run_table9(args):
                     "hbm_frac": round(by / (med * 1e-6) / 1e9 / peak, 4),
                     "peak_source": f"{peak_kind} hbm_gbs",
                     "c4r4_vs_bf16_pct": (round(100.0 * (res[4] - med) / med, 1)
-                                         if cb == 16 and 4 in res else None)}), flush=True)
+                                         if cb == 16 and 4 in res else None),
+                    # every call's time, so that runs in separate processes can be
+                    # pooled (the Table 9 entries average 120 samples of two runs)
+                    "samples_us": [round(t, 2) for t in ts]}), flush=True)
                 del cache, ws, out, q
                 torch.cuda.empty_cache()
 
