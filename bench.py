@@ -320,6 +320,17 @@ def config_record(w: syn.Workload, lens, ms, peak, tpk, kind: str):
            "packed_cache_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
            "tensor_tflops": round(tf, 2), "tensor_frac": round(tf / tpk, 4),
            "bound": "tensor" if tensor_bound else "hbm", "kernel": kind}
+    # the same roofline object as the headline's, for this workload's bound
+    trec = traffic_record(f"decode_{w.name}")
+    rec["roofline"] = {
+        "bound": rec["bound"], "kernel": kind,
+        "achieved": round(tf, 2) if tensor_bound else round(gbs, 1),
+        "peak": tpk if tensor_bound else peak,
+        "unit": "TFLOP/s" if tensor_bound else "GB/s",
+        "frac": rec["tensor_frac"] if tensor_bound else rec["hbm_frac"],
+        "traffic": (trec or {}).get("dram_bytes_per_launch"),
+        "traffic_source": (f"ncu capture: {trec.get('source')}" if trec else
+                           "no ncu capture of the current kernel sources (null)")}
     return rec
 
 
@@ -394,7 +405,7 @@ def run_gpu(args, w):
     dec_tflops = algorithmic_flops(ws_, s.lens) / (t_step * 1e-3) / 1e12
     tensor_bound = head["bound"] == "tensor"
     traffic = {"traffic": (trec or {}).get("dram_bytes_per_launch"),
-               "traffic_source": (f"ncu capture: {trec.get('profile')}" if trec else
+               "traffic_source": (f"ncu capture: {trec.get('source')}" if trec else
                                   "no ncu capture of the current kernel sources (null)")}
     roofline = ({"bound": "tensor", "kernel": kernel_desc, "achieved": round(dec_tflops, 2),
                  "peak": tpk, "peak_source": f"{tpk_kind} bf16_tflops (fp16 runs at the same rate)",
