@@ -45,11 +45,11 @@
 // tile three back; bf16 pages run 64-token tiles in a 4-deep ring.
 //
 // Warp roles (448 threads, one CTA per SM):
-//   warps 0-3   unpack: two threads per token of the tile (one per half of the
-//               CTA's groups; warps 0-2 for 48-token tiles); the next tile's
-//               bytes are loaded into registers while a plane buffer drains
-//               (bf16 pages: one thread issues the tensor copies, the warps
-//               clear rows past the sequence);
+//   warps 0-3   unpack: two threads per token (one per half of the CTA's
+//               groups), 64 tokens (a page) per step into 48-token tiles; the
+//               next page's bytes are loaded into registers while a plane
+//               buffer drains (bf16 pages: one thread issues the tensor copies,
+//               the warps clear rows past the sequence);
 //   warps 4-11  softmax: TMEM lane quadrant w & 3 (32 rows), token half
 //               (w - 4) >> 2 (24 or 32 tokens);
 //   warp 12     QK issue (one lane) and the TMEM allocation;
@@ -553,19 +553,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // copies issued but not waited for (an early exit) land before the CTA leaves
     if (tid == 0)
       for (int i = consumed; i < issued; ++i) drain_wait(bar(kBarTFull + i % NB), (i / NB) & 1, a.wait_cycles);
-  } else if (warp < 4 && (tid >> 1) < TOK) {
-    // ---------------- unpack: token t of every tile (warps 0-2: 48 tokens);
-    // thread half gh takes content groups 2gh, 2gh+1 and RoPE words 4r+2gh,
-    // 4r+2gh+1 (16 channels).  Tile i holds tokens 48i .. 48i+47 of the
-    // split's run of pages, so a tile can span two pages.
-    const int t = tid >> 1, gh = tid & 1;
+  } else if (warp < 4) {
+    // ---------------- unpack, over the split's tokens in batches of 64 (batch
+    // b of the run of pages is page b): token u of every batch, two threads
+    // per token; thread half gh takes content groups 2gh, 2gh+1 and RoPE words
+    // 4r+2gh, 4r+2gh+1 (16 channels).  Position s = 64b + u is row s mod 48 of
+    // tile s / 48, so a tile spans two batches; a warp's 16 tokens always lie
+    // in one tile (48 and 64 are multiples of 16) and it waits for that tile's
+    // buffer alone.
+    const int u = tid >> 1, gh = tid & 1;
     uint4 nc[4];
     uint2 nr = make_uint2(0, 0);
     uint32_t nm[3];
     bool n_ok = false, n_okt = false;
-    auto fetch = [&](int i) {
-      const int rel = TOK * i + t;  // token of the split's run of pages
-      const int pi = rel >> 6, row = rel & (kPageTokens - 1);
+    auto fetch = [&](int pi) {  // row u of page pi of the split's run
+      const int row = u;
       const bool in_run = pi < n_pk;
       const long long page = in_run ? s_pages[pi] : 0;
       const int pos = (sw.page_begin + pi) * kPageTokens + row;
@@ -603,8 +605,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         nm[2] = *reinterpret_cast<const uint32_t*>(mrow + 32);
       }
     };
-    if (n_pt > 0) fetch(0);
-    for (int i = 0; i < n_tiles; ++i) {
+    if (u < TOK * n_pt) fetch(0);
+    for (int bb = 0;; ++bb) {
+      const int s = 64 * bb + u;  // position in the split's tiles
+      if (s >= TOK * n_tiles) break;
+      const int i = s / TOK, t = s - i * TOK;  // tile, row
       const int buf = i % NB;
       uint4 cc[4];
 #pragma unroll
@@ -612,7 +617,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint2 rr = nr;
       const uint32_t mw0 = nm[0], mw1 = nm[1], mw2 = nm[2];
       const bool okt_cur = n_okt;
-      if (i + 1 < n_pt) fetch(i + 1);  // in flight while the buffer drains
+      if (s + 64 < TOK * n_pt) fetch(bb + 1);  // in flight while the buffer drains
       const bool packed = i < n_pt;
       // What needs only this tile's metadata is done before the buffer is
       // free: the token factor, the scale parts, m', the min-term chunks, the
@@ -797,7 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(A + 4 * PL + tc::sw_chunk(t, 4 * (1 - r) + 2 * gh + c2)) =
               make_uint4(0, 0, 0, 0);
       }
-      if (lane == 0) sMask[buf * 4 + warp] = mk | (any_shift ? 0x80000000u : 0u);
+      if (lane == 0) sMask[buf * 4 + t / 16] = mk | (any_shift ? 0x80000000u : 0u);
       tc::fence_async_smem();
       // self-test of the bounded waits: the first tile's hand-off is withheld
       if (!(a.fault == 1 && i == 0)) tc::bar_arrive(bar(kBarAFull + buf));
@@ -1002,17 +1007,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // (the max of the raw logits, scaled once: the scale is positive and
       // rounding is monotonic, so this is the max of the scaled logits)
-      float mx = -INFINITY;
+      // (four independent chains: the max does not depend on the order)
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (vmask == kAll) {
 #pragma unroll
-        for (int t = 0; t < TW; ++t) mx = fmaxf(mx, S[t]);
+        for (int t = 0; t < TW; ++t) mx4[t & 3] = fmaxf(mx4[t & 3], S[t]);
       } else {
 #pragma unroll
         for (int t = 0; t < TW; ++t) {
           S[t] = ((vmask >> t) & 1u) ? S[t] : -INFINITY;
-          mx = fmaxf(mx, S[t]);
+          mx4[t & 3] = fmaxf(mx4[t & 3], S[t]);
         }
       }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       sMax[((i & 1) * 2 + th) * kRows + h] = mx * a.scale_log2;
       if (pair_any(!ok, qd)) break;  // both warps of the rows leave at the same tile
       // my reads of the peer's partial are done: one arrival per warp, issued
@@ -1046,13 +1053,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // p = 2^(scale * S - m) in one rounding; masked tokens (S = -inf) give 0,
       // also while no token of the row has been valid yet (m = -inf)
       const float mneg = m_run == -INFINITY ? 0.f : -m_run;
-      float lsum = 0.f;
+      // (the tile's sum in four partial sums: short dependency chains)
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int t = 0; t < TW; ++t) {
         S[t] = fast_exp2(fmaf(S[t], a.scale_log2, mneg));
-        lsum += S[t];
+        ls4[t & 3] += S[t];
       }
-      l += lsum;
+      l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       // min terms of my four PV groups (unscaled P).  The loop stays rolled
       // (the per-tile code of all warp roles has to fit the instruction
       // caches): the four sums rotate one place per group, back in order
