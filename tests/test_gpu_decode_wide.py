@@ -218,3 +218,31 @@ def test_min_terms_with_q_group_sums_beyond_fp16(heads):
     ref, ref_lse = oracle.mla_decode_fp64(q_b, model.effective_keys(0, L), scale)
     check_attention(got, ref, f"{heads} heads")
     assert np.allclose(lse.cpu().numpy()[0], ref_lse, rtol=0, atol=1e-3)
+
+
+def _lengths_for_chunk(lay, chunk, num_sms, batch=2):
+    """Equal sequence lengths for which the planner cuts 128-head work into splits
+    of `chunk` pages (found with the library's own planner for this GPU's SM count)."""
+    import bit_mla_kv_lowbit_gb300 as pkg
+    for L in range(2000, 60000, 64):
+        if pkg.decode_plan(lay, 128, [L] * batch, num_sms=num_sms)[1] == chunk:
+            return [L] * batch
+    return None
+
+
+@pytest.mark.parametrize("chunk", [2, 3, 4, 5])
+def test_wide_tiles_spanning_pages(chunk):
+    # Packed caches run 48-token tiles over a split's pages: with `chunk` pages
+    # per split (64 * chunk tokens) the tiles cross page boundaries at 16, 32 or
+    # 0 tokens in and the last tile of a split is ragged for chunk = 1, 2, 4, 5.
+    # Every split size from 2 to 5 pages, checked against the oracle.
+    import torch
+    import bit_mla_kv_lowbit_gb300 as pkg
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    lens = _lengths_for_chunk(pkg.layout(4, 4), chunk, nsm)
+    if lens is None:
+        pytest.skip(f"no length gives {chunk}-page splits on {nsm} SMs")
+    w = syn.custom(f"wide_span_k{chunk}", lens, heads=128, content_bits=4, seed=90 + chunk)
+    run = GpuRun(w)
+    run.prefill()
+    _check_run_step(run, 0, lse=True)
