@@ -42,3 +42,34 @@ def test_random_config(seed):
 def test_draws_cover_both_kernels_and_every_layout():
     draws = [_draw(s) for s in range(12)]
     assert {(d[0], d[2]) for d in draws} == {(cb, h) for cb, _ in LAYOUTS for h in HEADS}
+
+
+# multi-token query decode: (layout, heads, queries per sequence) so that the
+# query rows per sequence are 32, 64 (16-row kernel) and 128, 256 (cluster kernel)
+MULTI = [(4, 16, 2), (2, 16, 4), (4, 16, 8), (16, 32, 4), (4, 128, 2), (2, 64, 2)]
+
+
+@pytest.mark.parametrize("case", range(len(MULTI)))
+def test_random_multi_query(case):
+    from tests.test_gpu_decode_multi import _run_multi
+    cb, heads, n = MULTI[case]
+    rng = np.random.default_rng(2000 + case)
+    batch = int(rng.integers(1, 4))
+    # every sequence holds at least its n query tokens
+    lens = np.exp(rng.uniform(np.log(n), np.log(6000.0), batch)).astype(int).clip(n, 6000)
+    _run_multi(cb, heads, n, [int(x) for x in lens], seed=300 + case)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_rotated(seed):
+    # the rotated cache (writer rotation, rotated queries, output rotated back)
+    rng = np.random.default_rng(3000 + seed)
+    cb = (4, 2)[seed % 2]
+    heads = (16, 128)[seed // 2]
+    batch = int(rng.integers(1, 4))
+    lens = np.exp(rng.uniform(0.0, np.log(6000.0), batch)).astype(int).clip(1, 6000)
+    w = syn.custom(f"randrot{seed}_c{cb}_h{heads}", [int(x) for x in lens], heads=heads,
+                   content_bits=cb, seed=400 + seed)
+    run = GpuRun(w, rotate=True)
+    run.prefill()
+    _check_run_step(run, 0, lse=True)
